@@ -1,0 +1,191 @@
+/*
+ * pkv.h — C ABI of libpkv: attention over a paged KV cache for one
+ * continuous-batching step, on one GB300 (sm_103a).
+ *
+ * What the operations are (the source pages name them, they print no API):
+ *  - "Efficient management of attention key and value memory with
+ *    PagedAttention" (Welcome to vLLM, feature list): K/V of every sequence
+ *    live in fixed-size physical blocks reached through a per-sequence block
+ *    table; "per-step KV bookkeeping handed to the kernels" (Litellama,
+ *    Architecture tree, executor/attention_metadata.py).
+ *  - "flash attention decode (online softmax, paged KV, GQA)" and
+ *    "Split-KV paged attention for long context" (rvLLM: High-performance
+ *    LLM inference in Rust, Kernel Compiler Stack / Tier 2: Hand-written CUDA
+ *    kernels; FA3 v3 Attention Kernel).
+ *  - partial attention "merged by log-sum-exp" (rapid_llm README, feature
+ *    table, row "Decode context parallelism"), done here over KV partitions
+ *    of one GPU.
+ *  - "RoPE + KV cache write" (rvLLM, Kernel Compiler Stack, decode step at
+ *    c=128): the cache-write half is reshape_and_cache below.
+ *  - "FP8 KV Cache" (Litellama, Features; rvLLM, Optional Features):
+ *    E4M3 codes with one fp32 scale per KV head for K and one for V.
+ *  - "Chunked Prefill ... 512-token chunks" (Litellama, Features): causal
+ *    attention of a chunk of new query tokens over the same paged cache.
+ *
+ * Conventions shared by every entry point
+ *  - All pointers are DEVICE pointers unless stated; the caller owns every
+ *    buffer. The library allocates no device memory and keeps no per-call
+ *    state; the only library-wide state is one device error word and a
+ *    cached per-device SM count.
+ *  - `stream` is a cudaStream_t passed as an opaque pointer (NULL = the
+ *    legacy default stream). Work is only enqueued; nothing synchronises,
+ *    except pkv_get_device_error.
+ *  - Argument checks are synchronous: a bad argument returns a status and
+ *    nothing is launched. A launch failure returns PKV_ERR_CUDA.
+ *  - Data-dependent checks run on the device (block ids outside
+ *    [0, num_blocks), slots outside the pool, seq_lens above the stated
+ *    maximum). A failing check skips the access, sets a bit in the device
+ *    error word and never traps; pkv_get_device_error reads the word.
+ *  - Tensors are dense and row-major. Every base pointer must be 16-byte
+ *    aligned.
+ *  - Layouts (B = num_seqs, Hq = num_q_heads, Hkv = num_kv_heads,
+ *    G = Hq / Hkv, D = head_dim, BS = block_size):
+ *      q            [B, Hq, D]                       q dtype
+ *      out          [B, Hq, D]                       q dtype
+ *      k_cache      [num_blocks, Hkv, BS, D]          kv dtype (same for v)
+ *      block_tables int32 [B, max_blocks_per_seq]
+ *      seq_lens     int32 [B]  context length INCLUDING the new token, whose
+ *                              K/V reshape_and_cache has already written
+ *    Logical token j of sequence b lives in physical block
+ *    block_tables[b][j / BS] at offset j % BS. Query head h reads KV head
+ *    h / G. Within a block each KV head's BS x D page is one contiguous run.
+ *  - Supported: D in {64, 128}; BS == 16; G <= 16; q dtype F16 or BF16; KV
+ *    dtype equal to the q dtype, or FP8_E4M3 with per-KV-head fp32 scales
+ *    (dequantised value = code * scale).
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer */
+  PKV_ERR_UNSUPPORTED = 2,   /* valid but not built: D, BS, G or dtype pair */
+  PKV_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+  PKV_ERR_CUDA = 4,          /* a CUDA runtime call or a launch failed */
+  PKV_ERR_DEVICE_CHECK = 5   /* a device-side check failed (see below) */
+} pkv_status;
+
+typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
+
+/* Bits of the device error word. */
+#define PKV_DEVERR_BLOCK_ID   0x1u  /* block table entry outside [0, num_blocks) */
+#define PKV_DEVERR_SLOT       0x2u  /* slot >= num_blocks * block_size */
+#define PKV_DEVERR_SEQ_LEN    0x4u  /* seq_len < 0 or above the stated maximum */
+#define PKV_DEVERR_TIMEOUT    0x8u  /* a bounded wait on an async copy gave up */
+#define PKV_DEVERR_QLEN       0x10u /* prefill: chunk longer than its context */
+
+/*
+ * paged_attn_decode_workspace_size
+ *   Bytes of device workspace paged_attn_decode needs for these sizes
+ *   (fp32 partial outputs and log-sum-exps of the split-KV partitions).
+ *   partition_tokens: as passed to paged_attn_decode (0 = automatic; the
+ *   automatic choice depends on the current device's SM count, so query on
+ *   the device that will run the call). Returns 0 for invalid sizes.
+ */
+size_t paged_attn_decode_workspace_size(int num_seqs, int num_q_heads,
+                                        int num_kv_heads, int head_dim,
+                                        int max_seq_len, int partition_tokens);
+
+/*
+ * paged_attn_decode — one query token per sequence against its paged K/V.
+ *   For each sequence b and query head h (KV head g = h / G):
+ *     s_j   = scale * k_scale[g] * <q[b,h,:], Kcode_j>          j < seq_lens[b]
+ *     out   = v_scale[g] * sum_j softmax(s)_j * Vcode_j          (q dtype, RNE)
+ *     lse   = log(sum_j exp(s_j))                                (natural log)
+ *   (k_scale = v_scale = 1 unless kv_dtype is FP8_E4M3.)
+ *   The context is cut into partitions of `partition_tokens` tokens
+ *   (multiple of 16, or 0 = automatic); each partition is reduced with an
+ *   online softmax and the partitions are merged by log-sum-exp.
+ *   seq_lens[b] == 0 gives out = 0 and lse = -inf.
+ *   max_seq_len: upper bound on every seq_lens[b] (sizes the grid); a larger
+ *   seq_len sets PKV_DEVERR_SEQ_LEN and is clamped.
+ *   k_scales, v_scales: fp32 [Hkv], required for FP8 KV, ignored otherwise.
+ *   out_lse: optional fp32 [B, Hq] (NULL to skip).
+ *   workspace: device buffer of at least paged_attn_decode_workspace_size()
+ *   bytes; its contents need no initialisation and are clobbered.
+ */
+pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype,
+                             const void* k_cache, const void* v_cache,
+                             pkv_dtype kv_dtype, const int32_t* block_tables,
+                             const int32_t* seq_lens, int num_seqs,
+                             int num_q_heads, int num_kv_heads, int head_dim,
+                             int block_size, int max_blocks_per_seq,
+                             int num_blocks, int max_seq_len, float scale,
+                             const float* k_scales, const float* v_scales,
+                             int partition_tokens, float* out_lse,
+                             void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/*
+ * paged_attn_prefill_chunk — causal attention of a chunk of new query
+ * tokens of each sequence over that sequence's paged cache.
+ *   Sequence n owns query rows cu_q_lens[n] .. cu_q_lens[n+1]-1 of q/out
+ *   ([total_q_tokens, Hq, D]); its chunk length L_n = cu_q_lens[n+1] -
+ *   cu_q_lens[n] and seq_lens[n] is its whole context INCLUDING the chunk
+ *   (whose K/V reshape_and_cache has already written), so P_n = seq_lens[n]
+ *   - L_n tokens precede it. Query row i of the chunk sits at absolute
+ *   position P_n + i and attends keys 0 .. P_n + i (causal, aligned to the
+ *   bottom right). Same scores, scales and output dtype as decode.
+ *   max_q_len: upper bound on every L_n (sizes the grid).
+ *   out_lse: optional fp32 [total_q_tokens, Hq].
+ *   A chunk with L_n > seq_lens[n] sets PKV_DEVERR_QLEN and is skipped.
+ */
+pkv_status paged_attn_prefill_chunk(void* out, const void* q,
+                                    pkv_dtype q_dtype, const void* k_cache,
+                                    const void* v_cache, pkv_dtype kv_dtype,
+                                    const int32_t* block_tables,
+                                    const int32_t* seq_lens,
+                                    const int32_t* cu_q_lens, int num_seqs,
+                                    int total_q_tokens, int max_q_len,
+                                    int num_q_heads, int num_kv_heads,
+                                    int head_dim, int block_size,
+                                    int max_blocks_per_seq, int num_blocks,
+                                    float scale, const float* k_scales,
+                                    const float* v_scales, float* out_lse,
+                                    void* stream);
+
+/*
+ * reshape_and_cache — write the K/V rows of new tokens into their slots.
+ *   key, value: [num_tokens, Hkv, D] in src_dtype (F16 or BF16).
+ *   slot_mapping: int64 [num_tokens]; slot s names block s / BS, offset
+ *   s % BS; s < 0 means "write nothing" (padding tokens).
+ *   For every token t and KV head h, the D values land in
+ *   k_cache[s / BS][h][s % BS][:] (same for v_cache):
+ *     kv_dtype == src_dtype : bit copy
+ *     kv_dtype == FP8_E4M3  : code = E4M3(x / k_scales[h]) with the division
+ *                             done as one correctly rounded fp32 operation
+ *                             and the conversion rounding to nearest even,
+ *                             saturating at +-448 (NaN stays NaN).
+ *   A slot >= num_blocks * BS sets PKV_DEVERR_SLOT and is skipped.
+ */
+pkv_status reshape_and_cache(const void* key, const void* value,
+                             pkv_dtype src_dtype, void* k_cache, void* v_cache,
+                             pkv_dtype kv_dtype, const int64_t* slot_mapping,
+                             int num_tokens, int num_kv_heads, int head_dim,
+                             int block_size, int num_blocks,
+                             const float* k_scales, const float* v_scales,
+                             void* stream);
+
+/*
+ * pkv_get_device_error — synchronises `stream`, then reads and clears the
+ * device error word of the current device. Returns PKV_OK when no check
+ * failed since the last read, else PKV_ERR_DEVICE_CHECK with the PKV_DEVERR_*
+ * bits in *bits (bits may be NULL). PKV_ERR_CUDA if the sync fails.
+ */
+pkv_status pkv_get_device_error(void* stream, unsigned int* bits);
+
+/* Static, human-readable name of a status. */
+const char* pkv_status_string(pkv_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */
