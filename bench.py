@@ -1,0 +1,541 @@
+#!/usr/bin/env python
+"""Benchmark of one attention-layer pass of a continuous-batching decode step
+over a paged KV cache: reshape_and_cache of the step's new tokens, then decode
+attention (split-KV partitions + log-sum-exp merge), on synthetic inputs.
+
+Metric: KV-read GB/s = algorithmic K+V bytes of the step (every context token
+of every sequence, per KV head, K and V) / device time of the step; also
+reported as seqs/s per layer and as a fraction of the HBM roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py --impl reference ...    # the fp64 CPU oracle, bounded sample
+
+Prints one JSON line (rank 0). Under torchrun each rank runs its own replica
+(weak scaling: one independent batch per GPU, no collective on the data path);
+the timed region is bracketed by a barrier and device syncs and the slowest
+rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import BENCH_CONFIG, CONFIGS, empty_cache, make_case  # noqa: E402
+
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASON_NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default=BENCH_CONFIG, choices=sorted(CONFIGS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work budget of the oracle baseline sample")
+    return ap.parse_args()
+
+
+# ---- distributed plumbing ---------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce(x: float, op: str, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---- clocks -----------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples of this GPU while running."""
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        sel = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            sel = vis.split(",")[device_index] if vis else str(device_index)
+        self.sel = sel
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu=timestamp,{CLOCK_QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", self.sel], stdout=open(self.path, "w"),
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 10:
+                        rows.append(parts)
+            os.unlink(self.path)
+        return rows
+
+    @staticmethod
+    def summarise(rows, t0_wall, t1_wall):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm, smax, reasons, n = [], None, set(), 0
+        for r in rows:
+            try:
+                sm.append(float(r[2]))
+                smax = float(r[3])
+            except ValueError:
+                continue
+            n += 1
+            for name, val in zip(REASON_NAMES, r[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        # samples under load: clocks above the idle floor
+        load = [x for x in sm if smax and x > 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ---- profile-derived traffic ----------------------------------------------------
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_decode_11_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(config: str):
+    """DRAM bytes per decode-attention call from the committed ncu summary of
+    this workload, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"decode_attention.{config}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    mh = re.search(r"source_hash:\s*([0-9a-f]+)", txt)
+    mt = re.search(r"dram_bytes_per_call:\s*([0-9]+)", txt)
+    if not mh or not mt or mh.group(1) != source_hash():
+        return None
+    return int(mt.group(1))
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---- workload helpers ---------------------------------------------------------------
+
+def workload_desc(case) -> str:
+    cfg = case.cfg
+    ctx = cfg["ctx"]
+    ctxs = (f"ctx U[{ctx[1]},{ctx[2]}]" if ctx[0] == "uniform" else
+            "ctx {" + ",".join(str(x) for x in ctx[1]) + "}")
+    kv = "E4M3 KV + per-head fp32 scales" if case.kv_fp8 else f"{case.dtype} KV"
+    s = (f"{case.name} decode step: reshape_and_cache of {len(case.new_slots)} new tokens + "
+         f"paged decode attention, B{case.B} Hq{case.Hq} Hkv{case.Hkv} D{case.D} block 16, "
+         f"{ctxs}, {case.dtype} q, {kv}, pool {case.num_blocks} blocks")
+    if case.prefill is not None:
+        s += f" + prefill chunk L{case.prefill.L} on P{case.prefill.P} (second stream)"
+    if cfg.get("shared_prefix"):
+        s += f"; {cfg['shared_prefix'][0]} seqs share a {cfg['shared_prefix'][1]}-token prefix"
+    return s
+
+
+def step_kv_bytes(case):
+    """(bytes counted for the metric, logical bytes) of one step."""
+    if case.cfg.get("shared_prefix"):
+        return case.kv_bytes_unique(), case.kv_bytes_logical()
+    return case.kv_bytes_logical(), case.kv_bytes_logical()
+
+
+def sample_units(case, n_units, rng):
+    """n (sequence, KV head) units of the workload, drawn without replacement."""
+    all_units = [(b, h) for b in range(case.B) for h in range(case.Hkv)]
+    idx = rng.choice(len(all_units), size=min(n_units, len(all_units)), replace=False)
+    return [all_units[i] for i in idx]
+
+
+def oracle_setup(case, units):
+    """The oracle's cache holding the rows the sampled sequences read."""
+    from oracle import oracle as O
+    seqs = sorted({b for b, _ in units})
+    kc, vc = empty_cache(case, "cpu")
+    slots_all = np.concatenate([case.fill_slots, case.new_slots])
+    rows = np.unique(np.concatenate(
+        [case.logical_rows(case.block_tables[b], int(case.seq_lens[b])) for b in seqs]))
+    nf = len(case.fill_slots)
+    rt = torch.as_tensor(rows)
+    fr, nr = rt[rt < nf], rt[rt >= nf] - nf
+    k = torch.cat([case.fill_k[fr.to(case.fill_k.device)].cpu(),
+                   case.new_k[nr.to(case.new_k.device)].cpu()]).contiguous()
+    v = torch.cat([case.fill_v[fr.to(case.fill_v.device)].cpu(),
+                   case.new_v[nr.to(case.new_v.device)].cpu()]).contiguous()
+    sl = np.concatenate([slots_all[fr.numpy()], slots_all[nf + nr.numpy()]])
+    assert O.reshape_and_cache(k, v, kc, vc, sl, case.k_scales, case.v_scales) == 0
+    return kc, vc
+
+
+def oracle_unit(case, kc, vc, unit, q_cpu):
+    from oracle import oracle as O
+    b, h = unit
+    G = case.G
+    O.decode(q_cpu, kc, vc, case.block_tables, case.seq_lens, case.scale, case.k_scales,
+             case.v_scales, sel=[b], heads=(h * G, (h + 1) * G))
+    return int(case.seq_lens[b]) * case.D * 2 * case.kv_elem_bytes
+
+
+def cpu_baseline(case, seconds: float, seed: int):
+    """The oracle as it stands, on a bounded sample of (sequence, KV head)
+    units of this workload, on the host cores; KV-read GB/s."""
+    from oracle import oracle as O
+    O.build()
+    O.set_threads(0)
+    rng = np.random.default_rng(seed + 99)
+    units = sample_units(case, case.B * case.Hkv, rng)
+    q_cpu = case.q.cpu().contiguous()
+    # size the sample: time one unit, then take what fits the budget
+    kc, vc = oracle_setup(case, units[:1])
+    t = time.perf_counter()
+    oracle_unit(case, kc, vc, units[0], q_cpu)
+    t1 = max(time.perf_counter() - t, 1e-4)
+    n = int(max(1, min(len(units), seconds / t1)))
+    units = units[:n]
+    kc, vc = oracle_setup(case, units)
+    nbytes = 0
+    t = time.perf_counter()
+    for u in units:
+        nbytes += oracle_unit(case, kc, vc, u, q_cpu)
+    dt = time.perf_counter() - t
+    return {"value": nbytes / dt / 1e9, "unit": "GB/s", "cores": O.threads(), "kind": "oracle",
+            "sample": f"{n} of {case.B * case.Hkv} (sequence, KV head) units of the same "
+                      f"workload, all {case.G} query heads of each, fp64 oracle, "
+                      f"{nbytes / 1e6:.1f} MB of KV in {dt:.2f} s"}
+
+
+# ---- our arm -------------------------------------------------------------------------------
+
+def run_ours(args):
+    rank, world, local = dist_setup()
+    torch.cuda.set_device(local)
+    from paged_kv_decode_11_gb300 import build as pkv_build
+    pkv_build.build()
+    import paged_kv_decode_11_gb300 as P
+    from paged_kv_decode_11_gb300.step import DecodeStep, MixedStep
+    P.load()
+
+    case = make_case(args.config, args.seed + rank, device="cuda")
+    kc, vc = empty_cache(case, "cuda")
+    ks = vs = None
+    if case.kv_fp8:
+        ks = torch.from_numpy(case.k_scales).cuda()
+        vs = torch.from_numpy(case.v_scales).cuda()
+    # the cache as the previous steps left it (every context token but the new ones)
+    P.reshape_and_cache(case.fill_k, case.fill_v, kc, vc,
+                        torch.from_numpy(case.fill_slots).cuda(), ks, vs)
+    torch.cuda.synchronize()
+    step = (MixedStep if case.prefill is not None else DecodeStep).from_case(case, kc, vc)
+    dstep = step.decode if isinstance(step, MixedStep) else step
+    decode_launches = 2 if dstep.workspace.numel() > 256 else 1
+    launches_per_step = 1 + decode_launches + (1 if case.prefill is not None else 0)
+    kv_bytes, kv_logical = step_kv_bytes(case)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def one_step():
+        step.run(stream)
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    assert P.pkv_get_device_error() == 0
+
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(K):
+        flush.fill_(i & 0xFF)                       # evict the previous step from L2
+        e0, ea, e1 = ev[i]
+        e0.record(stream)
+        if isinstance(step, MixedStep):
+            one_step()
+            ea.record(stream)                       # unused for the mixed step
+        else:
+            step.write_cache(stream)
+            ea.record(stream)
+            step.attend(stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    rows = sampler.stop() if rank == 0 else []
+    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    attn_ms = [b.elapsed_time(c) for _, b, c in ev] if not isinstance(step, MixedStep) else None
+    ms_local = float(np.mean(step_ms))
+    ms = allreduce(ms_local, "max", world)
+    total_bytes = allreduce(float(kv_bytes), "sum", world)
+    value = total_bytes / (ms / 1e3) / 1e9
+    total_seqs = allreduce(float(case.B), "sum", world)
+
+    # dominant kernel: the decode attention call (split kernel + merge) on this stream
+    peak, peak_kind = measured_hbm_peak()
+    if attn_ms is not None:
+        attn_mean = float(np.mean(attn_ms))
+        achieved = kv_bytes / (attn_mean / 1e3) / 1e9
+    else:
+        attn_mean, achieved = None, None
+    traffic = profile_traffic(args.config)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(step, stream, args, world, kv_bytes, flush)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case, args.cpu_seconds, args.seed)
+
+    clocks = ClockSampler.summarise(rows, t0, t1)
+    if rank == 0:
+        line = {
+            "metric": "paged-KV decode attn: KV-read GB/s (% of GB300 HBM peak); seqs/s per layer",
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms, 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": ("e4m3 KV dequantised to f16 for m16n8k16 MMA, fp32 accumulate"
+                      if case.kv_fp8 else f"{case.dtype} m16n8k16 MMA, fp32 accumulate"),
+            "data": "synthetic (seeded N(0,1) values, random block placement)",
+            "config": {
+                "workload": workload_desc(case),
+                "global_batch": int(total_seqs),
+                "kv_bytes_per_step": int(kv_bytes),
+                "kv_bytes_logical_per_step": int(kv_logical),
+                "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed); "
+                      f"the step reads {kv_bytes / 1e6:.0f} MB of KV",
+                "parallelism": f"replicas x{world} (independent batch per GPU)",
+            },
+            "seqs_per_s_per_layer": round(total_seqs / (ms / 1e3), 1),
+            "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+            "roofline": {
+                "kernel": "decode attention call (decode_split_kernel + decode_merge_kernel)",
+                "bound": "hbm",
+                "achieved": round(achieved, 2) if achieved else None,
+                "peak": peak,
+                "peak_kind": peak_kind,
+                "unit": "GB/s",
+                "frac": round(achieved / peak, 4) if achieved else None,
+                "traffic": traffic,
+                "algorithmic_bytes_per_launch": int(kv_bytes),
+                "mean_call_us": round(attn_mean * 1e3, 2) if attn_mean else None,
+            },
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clocks,
+            "gpu_launches": launches_per_step * K,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def measure_e2e(step, stream, args, world, kv_bytes, flush):
+    """The same step through the public API with inputs copied from pinned
+    host memory and outputs read back, every step, inside the timed region."""
+    dev_in = step.inputs()
+    dev_out = step.outputs()
+    host_in = [t.cpu().pin_memory() for t in dev_in]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def e2e_step():
+        for d, h in zip(dev_in, host_in):
+            d.copy_(h, non_blocking=True)
+        step.run(stream)
+        for d, h in zip(dev_out, host_out):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        e2e_step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = allreduce(float(np.mean([a.elapsed_time(b) for a, b in ev])), "max", world)
+    total = allreduce(float(kv_bytes), "sum", world)
+    return {"value": round(total / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms, 5)}
+
+
+# ---- reference arm: the fp64 oracle on the host cores ------------------------------------
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import oracle as O
+    O.build()
+    O.set_threads(0)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    case = make_case(args.config, args.seed, device=dev)
+    rng = np.random.default_rng(args.seed + 7)
+    units = sample_units(case, case.B * case.Hkv, rng)
+    q_cpu = case.q.cpu().contiguous()
+    # calibrate: units per step so the whole warmup + timed run stays within ~2 minutes
+    kc, vc = oracle_setup(case, units[:1])
+    t = time.perf_counter()
+    oracle_unit(case, kc, vc, units[0], q_cpu)
+    t1 = max(time.perf_counter() - t, 1e-4)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    per_step = int(max(1, min(len(units), budget / t1)))
+    need = min(len(units), per_step * (args.steps + args.warmup))
+    kc, vc = oracle_setup(case, units[:need])
+    cursor = 0
+
+    def ref_step():
+        nonlocal cursor
+        nb = 0
+        for _ in range(per_step):
+            nb += oracle_unit(case, kc, vc, units[cursor % need], q_cpu)
+            cursor += 1
+        return nb
+
+    for _ in range(args.warmup):
+        ref_step()
+    nbytes = 0
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        nbytes += ref_step()
+    dt = time.perf_counter() - t
+    value = nbytes / dt / 1e9
+    kv_bytes, _ = step_kv_bytes(case)
+    sample = (f"each step: {per_step} (sequence, KV head) unit(s) of the workload, all "
+              f"{case.G} query heads each, fp64 oracle ({nbytes / max(1, args.steps) / 1e6:.2f} MB "
+              f"of KV per step vs {kv_bytes / 1e6:.0f} MB for the whole step)")
+    line = {
+        "impl": "reference",
+        "metric": "paged-KV decode attn: KV-read GB/s (% of GB300 HBM peak); seqs/s per layer",
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) values, random block placement)",
+        "config": {"workload": workload_desc(case), "global_batch": case.B,
+                   "parallelism": "host cores (OpenMP)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": O.threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

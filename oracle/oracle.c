@@ -210,7 +210,9 @@ static void load_q(double* qd, const void* q, int q_dtype, int64_t row, int D) {
  * and merges the partitions by log-sum-exp:
  *   LSE = log sum_p exp(lse_p),  out = sum_p exp(lse_p - LSE) o_p,
  * with empty partitions (lse_p = -inf) weighted 0. part_tokens = 0 is the
- * unsplit definition. Returns 0, or -1 on an out-of-pool block id.
+ * unsplit definition. Only query heads h_lo .. h_hi-1 are computed (out is
+ * then [nsel, h_hi - h_lo, D]); pass 0 and Hq for all heads. Returns 0, or
+ * -1 on an out-of-pool block id.
  */
 int pkvo_decode(double* out, double* lse, const void* q, int q_dtype,
                 const void* k_cache, const void* v_cache, int kv_dtype,
@@ -218,14 +220,15 @@ int pkvo_decode(double* out, double* lse, const void* q, int q_dtype,
                 int B, int Hq, int Hkv, int D, int BS, int max_blocks,
                 int64_t num_blocks, double scale, const float* k_scales,
                 const float* v_scales, const int32_t* sel, int nsel,
-                int part_tokens) {
+                int part_tokens, int h_lo, int h_hi) {
   (void)B;
   int G = Hq / Hkv;
   int bad = 0;
-  int64_t total = (int64_t)nsel * Hq;
+  int nh = h_hi - h_lo;
+  int64_t total = (int64_t)nsel * nh;
 #pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
   for (int64_t w = 0; w < total; ++w) {
-    int i = (int)(w / Hq), h = (int)(w % Hq);
+    int i = (int)(w / nh), h = h_lo + (int)(w % nh);
     int b = sel ? sel[i] : i;
     int g = h / G;
     int n = seq_lens[b];

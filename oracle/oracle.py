@@ -57,7 +57,7 @@ def lib():
         L.pkvo_reshape_and_cache.argtypes = [P, P, I, P, P, I, P, I, I, I, I, I, P, P]
         L.pkvo_decode.restype = I
         L.pkvo_decode.argtypes = [P, P, P, I, P, P, I, P, P, I, I, I, I, I, I, I64, D,
-                                  P, P, P, I, I]
+                                  P, P, P, I, I, I, I]
         L.pkvo_prefill_chunk.restype = I
         L.pkvo_prefill_chunk.argtypes = [P, P, P, I, P, P, I, P, P, P, I, I, I, I, I, I,
                                          I64, D, P, P]
@@ -116,22 +116,24 @@ def reshape_and_cache(key, value, k_cache, v_cache, slots, k_scales=None, v_scal
 
 
 def decode(q, k_cache, v_cache, block_tables, seq_lens, scale, k_scales=None,
-           v_scales=None, sel=None, part_tokens: int = 0):
+           v_scales=None, sel=None, part_tokens: int = 0, heads=None):
     """fp64 decode attention. q [B, Hq, D]; caches [num_blocks, Hkv, BS, D].
-    Returns (out [nsel, Hq, D], lse [nsel, Hq]) for the selected sequences."""
+    Returns (out [nsel, nh, D], lse [nsel, nh]) for the selected sequences
+    and the query-head range `heads` = (lo, hi) (default: all heads)."""
     B, Hq, D = q.shape
+    h_lo, h_hi = (0, Hq) if heads is None else heads
     nb, hkv, bs, _ = k_cache.shape
     bt = _np(block_tables, np.int32)
     sl = _np(seq_lens, np.int32)
     sel_a = None if sel is None else _np(sel, np.int32)
     nsel = B if sel is None else len(sel_a)
-    out = np.zeros((nsel, Hq, D), np.float64)
-    lse = np.zeros((nsel, Hq), np.float64)
+    out = np.zeros((nsel, h_hi - h_lo, D), np.float64)
+    lse = np.zeros((nsel, h_hi - h_lo), np.float64)
     ks, vs = _np(k_scales, np.float32), _np(v_scales, np.float32)
     rc = lib().pkvo_decode(
         _ptr(out), _ptr(lse), _ptr(q), _DT[q.dtype], _ptr(k_cache), _ptr(v_cache),
         _DT[k_cache.dtype], _ptr(bt), _ptr(sl), B, Hq, hkv, D, bs, bt.shape[1], nb,
-        float(scale), _ptr(ks), _ptr(vs), _ptr(sel_a), nsel, int(part_tokens))
+        float(scale), _ptr(ks), _ptr(vs), _ptr(sel_a), nsel, int(part_tokens), h_lo, h_hi)
     if rc != 0:
         raise ValueError("oracle decode: block id outside the pool")
     return out, lse

@@ -1,0 +1,319 @@
+// api.cu — the extern "C" entry points of libpkv declared in include/pkv.h:
+// synchronous argument checks, TMA tensor maps over the paged cache,
+// split-KV partition planning, and the kernel launches.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#pragma GCC visibility push(default)
+#include "../../include/pkv.h"
+#pragma GCC visibility pop
+#include "launch.h"
+
+namespace pkv {
+
+// The device error word: kernels OR PKV_DEVERR_* bits into it; read and
+// cleared by pkv_get_device_error.
+__device__ unsigned int g_pkv_deverr;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+std::mutex g_mu;
+unsigned int* g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool current_device(int* dev) {
+  if (cudaGetDevice(dev) != cudaSuccess) return false;
+  return *dev >= 0 && *dev < kMaxDevices;
+}
+
+unsigned int* err_word() {
+  int dev;
+  if (!current_device(&dev)) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_pkv_deverr) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+int sm_count() {
+  int dev;
+  if (!current_device(&dev)) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sms[dev] = n;
+  }
+  return g_sms[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return g_encode;
+}
+
+// Tensor map {D, 16, num_blocks * Hkv} over a cache [num_blocks, Hkv, 16, D]:
+// one box is 16 page rows by min(row bytes, 128) bytes, swizzled so that
+// the fragment loads of the kernels are bank-conflict free.
+bool make_kv_tmap(CUtensorMap* m, const void* base, pkv_dtype dt, int D, int Hkv,
+                  int num_blocks) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const int elt = dt == PKV_FP8_E4M3 ? 1 : 2;
+  const int row_bytes = D * elt;
+  const int box_row = row_bytes > 128 ? 128 : row_bytes;
+  CUtensorMapDataType t = dt == PKV_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                          : dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                           : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  cuuint64_t dims[3] = {(cuuint64_t)D, 16, (cuuint64_t)num_blocks * (cuuint64_t)Hkv};
+  cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)row_bytes * 16};
+  cuuint32_t box[3] = {(cuuint32_t)(box_row / elt), 16, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, t, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  box_row == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Automatic split-KV partition size: enough (partition, KV head, sequence)
+// CTAs for about 16 per SM when the contexts average half the maximum,
+// between 256 and 1024 tokens (a power of two).
+int auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int sms) {
+  const int64_t est = (int64_t)num_seqs * num_kv_heads * (max_seq_len / 2 + 1);
+  const int64_t target = (int64_t)(sms > 0 ? sms : 148) * 16;
+  int part = 256;
+  while (part < 1024 && est / part > target) part *= 2;
+  return part;
+}
+
+int plan_partition(int num_seqs, int num_kv_heads, int max_seq_len, int partition_tokens) {
+  if (partition_tokens > 0) return partition_tokens;
+  return auto_partition(num_seqs, num_kv_heads, max_seq_len, sm_count());
+}
+
+bool valid_dtypes(pkv_dtype q, pkv_dtype kv) {
+  if (q != PKV_F16 && q != PKV_BF16) return false;
+  return kv == q || kv == PKV_FP8_E4M3;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+size_t paged_attn_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int max_seq_len, int partition_tokens) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      max_seq_len < 0 || partition_tokens < 0 || partition_tokens % 16 != 0 ||
+      partition_tokens > kMaxPartitionTokens)
+    return 0;
+  const int part = plan_partition(num_seqs, num_kv_heads, max_seq_len, partition_tokens);
+  const int64_t max_parts = max_seq_len > 0 ? (max_seq_len + part - 1) / part : 1;
+  if (max_parts <= 1) return 256;
+  const size_t rows = (size_t)num_seqs * num_q_heads * max_parts;
+  return align256(rows * head_dim * sizeof(float)) + align256(rows * sizeof(float));
+}
+
+pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const void* k_cache,
+                             const void* v_cache, pkv_dtype kv_dtype, const int32_t* block_tables,
+                             const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                             int num_kv_heads, int head_dim, int block_size,
+                             int max_blocks_per_seq, int num_blocks, int max_seq_len, float scale,
+                             const float* k_scales, const float* v_scales, int partition_tokens,
+                             float* out_lse, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_seq_len < 0 ||
+      max_blocks_per_seq <= 0 || num_blocks <= 0 || partition_tokens < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (partition_tokens % 16 != 0 || partition_tokens > kMaxPartitionTokens)
+    return PKV_ERR_INVALID_ARG;
+  if (!valid_dtypes(q_dtype, kv_dtype)) return PKV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (block_size != 16) return PKV_ERR_UNSUPPORTED;
+  const int G = num_q_heads / num_kv_heads;
+  if (G > 16) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens)
+    return PKV_ERR_INVALID_ARG;
+  if (kv_dtype == PKV_FP8_E4M3 && (!k_scales || !v_scales)) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+
+  const int part = plan_partition(num_seqs, num_kv_heads, max_seq_len, partition_tokens);
+  const int max_parts = max_seq_len > 0 ? (max_seq_len + part - 1) / part : 1;
+  DecodeParams p{};
+  if (max_parts > 1) {
+    const size_t rows = (size_t)num_seqs * num_q_heads * max_parts;
+    const size_t o_bytes = align256(rows * head_dim * sizeof(float));
+    const size_t need = o_bytes + align256(rows * sizeof(float));
+    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+      return PKV_ERR_WORKSPACE;
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
+  }
+  CUtensorMap tmK, tmV;
+  if (!make_kv_tmap(&tmK, k_cache, kv_dtype, head_dim, num_kv_heads, num_blocks) ||
+      !make_kv_tmap(&tmV, v_cache, kv_dtype, head_dim, num_kv_heads, num_blocks))
+    return PKV_ERR_CUDA;
+  unsigned int* err = err_word();
+  if (err == nullptr) return PKV_ERR_CUDA;
+  p.out = out;
+  p.q = q;
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.k_scales = k_scales;
+  p.v_scales = v_scales;
+  p.out_lse = out_lse;
+  p.err = err;
+  p.B = num_seqs;
+  p.Hq = num_q_heads;
+  p.Hkv = num_kv_heads;
+  p.G = G;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.max_seq_len = max_seq_len;
+  p.part = part;
+  p.max_parts = max_parts;
+  p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+  return launch_decode(p, head_dim, q_dtype, kv_dtype, tmK, tmV,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status paged_attn_prefill_chunk(void* out, const void* q, pkv_dtype q_dtype,
+                                    const void* k_cache, const void* v_cache, pkv_dtype kv_dtype,
+                                    const int32_t* block_tables, const int32_t* seq_lens,
+                                    const int32_t* cu_q_lens, int num_seqs, int total_q_tokens,
+                                    int max_q_len, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int block_size, int max_blocks_per_seq,
+                                    int num_blocks, float scale, const float* k_scales,
+                                    const float* v_scales, float* out_lse, void* stream) {
+  if (num_seqs < 0 || total_q_tokens < 0 || max_q_len < 0 || num_q_heads <= 0 ||
+      num_kv_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if (!valid_dtypes(q_dtype, kv_dtype)) return PKV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (block_size != 16) return PKV_ERR_UNSUPPORTED;
+  const int G = num_q_heads / num_kv_heads;
+  if (G > 16) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0 || total_q_tokens == 0 || max_q_len == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !cu_q_lens)
+    return PKV_ERR_INVALID_ARG;
+  if (kv_dtype == PKV_FP8_E4M3 && (!k_scales || !v_scales)) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  CUtensorMap tmK, tmV;
+  if (!make_kv_tmap(&tmK, k_cache, kv_dtype, head_dim, num_kv_heads, num_blocks) ||
+      !make_kv_tmap(&tmV, v_cache, kv_dtype, head_dim, num_kv_heads, num_blocks))
+    return PKV_ERR_CUDA;
+  unsigned int* err = err_word();
+  if (err == nullptr) return PKV_ERR_CUDA;
+  PrefillParams p{};
+  p.out = out;
+  p.q = q;
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.cu_q_lens = cu_q_lens;
+  p.k_scales = k_scales;
+  p.v_scales = v_scales;
+  p.out_lse = out_lse;
+  p.err = err;
+  p.num_seqs = num_seqs;
+  p.Hq = num_q_heads;
+  p.Hkv = num_kv_heads;
+  p.G = G;
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.max_q_len = max_q_len;
+  p.q_tile = prefill_q_tile(G);
+  p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+  return launch_prefill(p, head_dim, q_dtype, kv_dtype, tmK, tmV,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status reshape_and_cache(const void* key, const void* value, pkv_dtype src_dtype,
+                             void* k_cache, void* v_cache, pkv_dtype kv_dtype,
+                             const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                             int head_dim, int block_size, int num_blocks,
+                             const float* k_scales, const float* v_scales, void* stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+  if (!valid_dtypes(src_dtype, kv_dtype)) return PKV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (block_size != 16) return PKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  if (kv_dtype == PKV_FP8_E4M3 && (!k_scales || !v_scales)) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(key) || !aligned16(value) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PKV_ERR_INVALID_ARG;
+  unsigned int* err = err_word();
+  if (err == nullptr) return PKV_ERR_CUDA;
+  CacheWriteParams p{};
+  p.key = key;
+  p.value = value;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.slots = slot_mapping;
+  p.k_scales = k_scales;
+  p.v_scales = v_scales;
+  p.err = err;
+  p.num_tokens = num_tokens;
+  p.Hkv = num_kv_heads;
+  p.D = head_dim;
+  p.num_blocks = num_blocks;
+  return launch_cache_write(p, src_dtype, kv_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_get_device_error(void* stream, unsigned int* bits) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  unsigned int* err = err_word();
+  if (err == nullptr) return PKV_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return PKV_ERR_CUDA;
+  if (v != 0 && cudaMemset(err, 0, sizeof(v)) != cudaSuccess) return PKV_ERR_CUDA;
+  if (bits) *bits = v;
+  return v ? PKV_ERR_DEVICE_CHECK : PKV_OK;
+}
+
+const char* pkv_status_string(pkv_status s) {
+  switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_INVALID_ARG: return "invalid argument";
+    case PKV_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_CUDA: return "CUDA error";
+    case PKV_ERR_DEVICE_CHECK: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,240 @@
+// common.cuh — page geometry in shared memory and the warp-level fragment
+// routines that decode and prefill share.
+//
+// A KV page is the BS x D run of one KV head inside one physical block
+// (cache layout [num_blocks, Hkv, BS, D]); BS = 16 tokens. It reaches shared
+// memory through a 3-D TMA tensor map {D, BS, num_blocks * Hkv}, box
+// {BOX_ELEMS, 16, 1}, with the 128-byte (or 64-byte) swizzle, so a page is
+// NBOX boxes of 16 rows x BOX_ROW_BYTES bytes.
+//
+// QK^T and PV of one page are m16n8k16 tensor-core products with 16 query
+// rows (the GQA group, padded) and fp32 accumulators:
+//   S[16 x 16 tokens]  = Q[16 x D] . K_page^T        (2 n-tiles, D/16 k-steps)
+//   O[16 x D]         += P[16 x 16 tokens] . V_page   (D/8 n-tiles, 1 k-step)
+// 16-bit caches feed the B operands with ldmatrix (.trans for V). E4M3
+// caches are converted in registers (cvt e4m3x2 -> f16x2, exact) and use f16
+// MMAs; their operand layouts are chosen so every thread reads whole 16-byte
+// chunks without bank conflicts:
+//   * K: the contraction index d is permuted. Thread (g = lane/4, c = lane%4)
+//     reads chunk 4u + c (bytes 16(4u+c) .. +15) of its token row; byte pair
+//     (4i, 4i+1) feeds b0 and (4i+2, 4i+3) feeds b1 of k-step 4u + i. The Q
+//     fragments use the same permutation, so the dot products are unchanged.
+//   * tokens: B column n of a K n-tile is token pi(n) = n ^ ((n & 1) << 2);
+//     with the 128-byte swizzle this keeps both the K reads and the V reads
+//     of every 8-lane phase on distinct banks. S column n is token pi(n).
+//   * V: output column n of n-tile t is d = (D/8) n + t, so thread g reads
+//     the D/8 contiguous bytes starting at d = (D/8) g of two token rows and
+//     interleaves them with byte permutes into (token, token') pairs.
+#pragma once
+#include <cstdint>
+#include "ptx.cuh"
+
+namespace pkv {
+
+constexpr int kBS = 16;                 // tokens per block (page rows)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+enum KvKind { KV_F16 = 0, KV_BF16 = 1, KV_E4M3 = 2 };
+
+template <int D, int KV>
+struct PageGeom {
+  static constexpr int ELT = (KV == KV_E4M3) ? 1 : 2;
+  static constexpr int ROW_BYTES = D * ELT;
+  static constexpr int BOX_ROW_BYTES = ROW_BYTES > 128 ? 128 : ROW_BYTES;
+  static constexpr int NBOX = ROW_BYTES / BOX_ROW_BYTES;
+  static constexpr int BOX_ELEMS = BOX_ROW_BYTES / ELT;
+  static constexpr int BOX_BYTES = BOX_ROW_BYTES * kBS;
+  static constexpr int PAGE_BYTES = ROW_BYTES * kBS;
+  static constexpr int SWZ_MASK = BOX_ROW_BYTES / 16 - 1;   // 7: 128B swizzle, 3: 64B
+  static constexpr int KSTEPS = D / 16;
+  static constexpr int NTILES = D / 8;
+  static_assert(BOX_ROW_BYTES == 128 || BOX_ROW_BYTES == 64, "unsupported page row");
+
+  // Byte offset inside a swizzled box of row `r`, byte `x` of the row.
+  __device__ __forceinline__ static uint32_t swz(uint32_t r, uint32_t x) {
+    uint32_t off = r * BOX_ROW_BYTES + x;
+    return off ^ (((off >> 7) & SWZ_MASK) << 4);
+  }
+  // Byte offset inside a page of element (token r, dim d) (16-bit caches).
+  __device__ __forceinline__ static uint32_t elem_off(uint32_t r, uint32_t d) {
+    return (d / BOX_ELEMS) * BOX_BYTES + swz(r, (d % BOX_ELEMS) * ELT);
+  }
+};
+
+// Token (0..15) of S accumulator element e (0, 1) of n-tile j for a thread
+// with c = lane % 4.
+template <int KV>
+__device__ __forceinline__ int s_col_token(int j, int c, int e) {
+  int n = 2 * c + e;
+  if constexpr (KV == KV_E4M3) n ^= ((n & 1) << 2);
+  return 8 * j + n;
+}
+
+// Head dimension of O accumulator element e (0, 1) of n-tile t.
+template <int D, int KV>
+__device__ __forceinline__ int o_col_dim(int t, int c, int e) {
+  int n = 2 * c + e;
+  if constexpr (KV == KV_E4M3) return (D / 8) * n + t;
+  else return 8 * t + n;
+}
+
+// Q fragments (A operand, 16 rows x D) for the page products. rowg / rowg8
+// point at the D values of query rows g and g + 8 (nullptr = padding row, 0).
+// E4M3 caches use f16 MMAs: q is converted to f16 and the contraction index
+// follows the permutation described at the top of this file.
+template <int D, int KV, bool QBF16>
+__device__ __forceinline__ void load_q_frags(uint32_t (&qf)[D / 16][4], const void* rowg,
+                                             const void* rowg8, int lane) {
+  const int c = lane & 3;
+  auto ld2 = [&](const void* row, int d) -> uint32_t {
+    if (row == nullptr) return 0u;
+    uint32_t raw = *reinterpret_cast<const uint32_t*>(
+        static_cast<const uint16_t*>(row) + d);
+    if constexpr (KV == KV_E4M3 && QBF16) {
+      __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&raw);
+      float2 f = __bfloat1622float2(v);
+      return pack_f16x2(f.x, f.y);
+    } else {
+      return raw;
+    }
+  };
+#pragma unroll
+  for (int s = 0; s < D / 16; ++s) {
+    int d0, d1;
+    if constexpr (KV == KV_E4M3) {
+      const int u = s >> 2, i = s & 3;
+      d0 = 16 * (4 * u + c) + 4 * i;
+      d1 = d0 + 2;
+    } else {
+      d0 = 16 * s + 2 * c;
+      d1 = d0 + 8;
+    }
+    qf[s][0] = ld2(rowg, d0);
+    qf[s][1] = ld2(rowg8, d0);
+    qf[s][2] = ld2(rowg, d1);
+    qf[s][3] = ld2(rowg8, d1);
+  }
+}
+
+// acc[j0 + j][.] += Q . K_page^T for the two 8-token n-tiles j of the page
+// at shared-memory byte address kpage (j0 is a compile-time offset after
+// unrolling, so acc stays in registers).
+template <int D, int KV, int NJ>
+__device__ __forceinline__ void qk_page(float (&acc)[NJ][4], int j0,
+                                        const uint32_t (&qf)[D / 16][4], uint32_t kpage,
+                                        int lane) {
+  using Geo = PageGeom<D, KV>;
+  if constexpr (KV == KV_E4M3) {
+    const int g = lane >> 2, c = lane & 3;
+    const int tn = g ^ ((g & 1) << 2);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int tok = 8 * j + tn;
+#pragma unroll
+      for (int u = 0; u < D / 64; ++u) {
+        uint4 w = lds128(kpage + Geo::swz(tok, 16 * (4 * u + c)));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          uint32_t b0 = e4m3x2_to_f16x2(ws[i] & 0xFFFFu);
+          uint32_t b1 = e4m3x2_to_f16x2(ws[i] >> 16);
+          mma_f16(acc[j0 + j], qf[4 * u + i], b0, b1);
+        }
+      }
+    }
+  } else {
+    constexpr bool BF = (KV == KV_BF16);
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int tok = 8 * j + (lane & 7);
+#pragma unroll
+      for (int s2 = 0; s2 < D / 32; ++s2) {
+        uint32_t r[4];
+        ldmatrix_x4(r, kpage + Geo::elem_off(tok, 32 * s2 + 8 * (lane >> 3)));
+        mma16816<BF>(acc[j0 + j], qf[2 * s2], r[0], r[1]);
+        mma16816<BF>(acc[j0 + j], qf[2 * s2 + 1], r[2], r[3]);
+      }
+    }
+  }
+}
+
+// oacc[t][.] += P . V_page for the page at shared-memory byte address vpage;
+// pa is the A fragment of P (16 rows x 16 tokens of this page).
+template <int D, int KV>
+__device__ __forceinline__ void pv_page(float (&oacc)[D / 8][4], const uint32_t (&pa)[4],
+                                        uint32_t vpage, int lane) {
+  using Geo = PageGeom<D, KV>;
+  if constexpr (KV == KV_E4M3) {
+    const int g = lane >> 2, c = lane & 3;
+    const int t0 = 2 * c, t1 = (2 * c + 1) ^ 4;      // pi(2c), pi(2c+1)
+    constexpr int CH = D / 8;                        // bytes per thread per row
+    const uint32_t xo = CH * g;
+    uint32_t wa[CH / 4], wb[CH / 4], wc[CH / 4], wd[CH / 4];
+    if constexpr (CH == 16) {
+      uint4 a = lds128(vpage + Geo::swz(t0, xo));
+      uint4 b = lds128(vpage + Geo::swz(t1, xo));
+      uint4 cc = lds128(vpage + Geo::swz(8 + t0, xo));
+      uint4 d = lds128(vpage + Geo::swz(8 + t1, xo));
+      wa[0] = a.x; wa[1] = a.y; wa[2] = a.z; wa[3] = a.w;
+      wb[0] = b.x; wb[1] = b.y; wb[2] = b.z; wb[3] = b.w;
+      wc[0] = cc.x; wc[1] = cc.y; wc[2] = cc.z; wc[3] = cc.w;
+      wd[0] = d.x; wd[1] = d.y; wd[2] = d.z; wd[3] = d.w;
+    } else {
+      uint2 a = lds64(vpage + Geo::swz(t0, xo));
+      uint2 b = lds64(vpage + Geo::swz(t1, xo));
+      uint2 cc = lds64(vpage + Geo::swz(8 + t0, xo));
+      uint2 d = lds64(vpage + Geo::swz(8 + t1, xo));
+      wa[0] = a.x; wa[1] = a.y;
+      wb[0] = b.x; wb[1] = b.y;
+      wc[0] = cc.x; wc[1] = cc.y;
+      wd[0] = d.x; wd[1] = d.y;
+    }
+#pragma unroll
+    for (int i = 0; i < CH / 4; ++i) {
+      const uint32_t lo01 = __byte_perm(wa[i], wb[i], 0x5140);
+      const uint32_t lo23 = __byte_perm(wa[i], wb[i], 0x7362);
+      const uint32_t hi01 = __byte_perm(wc[i], wd[i], 0x5140);
+      const uint32_t hi23 = __byte_perm(wc[i], wd[i], 0x7362);
+      mma_f16(oacc[4 * i + 0], pa, e4m3x2_to_f16x2(lo01 & 0xFFFFu), e4m3x2_to_f16x2(hi01 & 0xFFFFu));
+      mma_f16(oacc[4 * i + 1], pa, e4m3x2_to_f16x2(lo01 >> 16), e4m3x2_to_f16x2(hi01 >> 16));
+      mma_f16(oacc[4 * i + 2], pa, e4m3x2_to_f16x2(lo23 & 0xFFFFu), e4m3x2_to_f16x2(hi23 & 0xFFFFu));
+      mma_f16(oacc[4 * i + 3], pa, e4m3x2_to_f16x2(lo23 >> 16), e4m3x2_to_f16x2(hi23 >> 16));
+    }
+  } else {
+    constexpr bool BF = (KV == KV_BF16);
+    const int tok = (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+    for (int t2 = 0; t2 < D / 16; ++t2) {
+      uint32_t r[4];
+      ldmatrix_x4_trans(r, vpage + Geo::elem_off(tok, 16 * t2 + 8 * (lane >> 4)));
+      mma16816<BF>(oacc[2 * t2], pa, r[0], r[1]);
+      mma16816<BF>(oacc[2 * t2 + 1], pa, r[2], r[3]);
+    }
+  }
+}
+
+// P operand of the page product, packed from the S n-tiles j0 and j0 + 1. 16-bit
+// caches use their own dtype for P; E4M3 caches use f16.
+template <int KV, int NJ>
+__device__ __forceinline__ void pack_p(uint32_t (&pa)[4], const float (&p)[NJ][4], int j0) {
+  constexpr bool BF = (KV == KV_BF16);
+  pa[0] = pack2<BF>(p[j0][0], p[j0][1]);
+  pa[1] = pack2<BF>(p[j0][2], p[j0][3]);
+  pa[2] = pack2<BF>(p[j0 + 1][0], p[j0 + 1][1]);
+  pa[3] = pack2<BF>(p[j0 + 1][2], p[j0 + 1][3]);
+}
+
+__device__ __forceinline__ float quad_max(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+  return v;
+}
+
+__device__ __forceinline__ float quad_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  v += __shfl_xor_sync(0xffffffffu, v, 2);
+  return v;
+}
+
+}  // namespace pkv

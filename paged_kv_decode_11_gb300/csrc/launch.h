@@ -1,0 +1,68 @@
+// launch.h — host-side parameter blocks and launchers shared by the
+// translation units of libpkv (not part of the public ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+constexpr int kMaxPartitionTokens = 8192;   // split-KV partition cap (block ids staged in smem)
+
+struct DecodeParams {
+  void* out;
+  const void* q;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  const float* k_scales;
+  const float* v_scales;
+  float* out_lse;
+  float* ws_o;          // [B, Hq, max_parts, D] fp32 partition outputs (normalised)
+  float* ws_lse;        // [B, Hq, max_parts]    fp32 partition log2-sum-exp
+  unsigned int* err;    // device error word
+  int B, Hq, Hkv, G, max_blocks, num_blocks, max_seq_len, part, max_parts;
+  float qk_scale_log2;  // scale * log2(e)
+};
+
+struct PrefillParams {
+  void* out;
+  const void* q;
+  const int32_t* block_tables;
+  const int32_t* seq_lens;
+  const int32_t* cu_q_lens;
+  const float* k_scales;
+  const float* v_scales;
+  float* out_lse;
+  unsigned int* err;
+  int num_seqs, Hq, Hkv, G, max_blocks, num_blocks, max_q_len, q_tile;
+  float qk_scale_log2;
+};
+
+struct CacheWriteParams {
+  const void* key;
+  const void* value;
+  void* k_cache;
+  void* v_cache;
+  const int64_t* slots;
+  const float* k_scales;
+  const float* v_scales;
+  unsigned int* err;
+  int num_tokens, Hkv, D, num_blocks;
+};
+
+// Each launcher validates nothing (the entry points do) and returns
+// PKV_ERR_CUDA on a launch failure.
+pkv_status launch_decode(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
+                         pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                         cudaStream_t stream);
+pkv_status launch_prefill(const PrefillParams& p, int head_dim, pkv_dtype q_dtype,
+                          pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                          cudaStream_t stream);
+pkv_status launch_cache_write(const CacheWriteParams& p, pkv_dtype src_dtype,
+                              pkv_dtype kv_dtype, cudaStream_t stream);
+
+// Rows of q handled by one prefill CTA for a GQA group size G.
+int prefill_q_tile(int G);
+
+}  // namespace pkv

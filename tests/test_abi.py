@@ -1,0 +1,129 @@
+"""The C-ABI library builds, loads and exports every symbol include/pkv.h
+declares; argument checks that need no GPU return their status codes. No
+compute call is made here (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_decode_11_gb300 as P
+from paged_kv_decode_11_gb300 import _binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pkv.h")
+
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
+F16, BF16, FP8 = 0, 1, 2
+FAKE = 0x10000          # never dereferenced: every call below fails its checks first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return P.load()
+
+
+def header_functions():
+    txt = open(HEADER).read()
+    txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", txt)) -
+                  {"if", "sizeof", "defined"})
+
+
+def test_header_declares_the_abi():
+    assert header_functions() == sorted(_binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_exports_nothing_else():
+    out = os.popen(f"nm -D --defined-only {_binding.LIB_PATH}").read()
+    syms = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    assert syms == set(header_functions())
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert P.pkv_status_string(s) == _binding.STATUS[s]
+    assert P.pkv_status_string(99) == "unknown status"
+
+
+def _decode(lib, **kw):
+    a = dict(out=FAKE, q=FAKE, q_dtype=BF16, k=FAKE, v=FAKE, kv_dtype=BF16, bt=FAKE, sl=FAKE,
+             B=4, Hq=8, Hkv=2, D=128, BS=16, maxb=8, nb=64, msl=128, scale=0.1, ks=None,
+             vs=None, part=0, lse=None, ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return lib.paged_attn_decode(a["out"], a["q"], a["q_dtype"], a["k"], a["v"], a["kv_dtype"],
+                                 a["bt"], a["sl"], a["B"], a["Hq"], a["Hkv"], a["D"], a["BS"],
+                                 a["maxb"], a["nb"], a["msl"], a["scale"], a["ks"], a["vs"],
+                                 a["part"], a["lse"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(D=96), UNSUPPORTED), (dict(BS=32), UNSUPPORTED), (dict(Hq=34, Hkv=2), UNSUPPORTED),
+    (dict(Hq=9, Hkv=2), INVALID), (dict(q_dtype=FP8, kv_dtype=FP8), UNSUPPORTED),
+    (dict(q_dtype=F16, kv_dtype=BF16), UNSUPPORTED), (dict(part=24), INVALID),
+    (dict(part=8192 + 16), INVALID), (dict(out=None), INVALID), (dict(bt=None), INVALID),
+    (dict(kv_dtype=FP8), INVALID), (dict(q=FAKE + 8), INVALID), (dict(B=-1), INVALID),
+    (dict(nb=0), INVALID), (dict(B=0, out=None), OK), (dict(B=70000), UNSUPPORTED),
+])
+def test_decode_argument_checks(lib, kw, want):
+    assert _decode(lib, **kw) == want
+
+
+def test_decode_workspace_check(lib):
+    # 2 partitions of 64 tokens: the workspace is required
+    assert _decode(lib, part=64, msl=128, ws=None) == WORKSPACE
+    need = P.paged_attn_decode_workspace_size(4, 8, 2, 128, 128, 64)
+    assert _decode(lib, part=64, msl=128, ws=FAKE, wsb=need - 1) == WORKSPACE
+
+
+def test_workspace_size_formula(lib):
+    # rows = B * Hq * parts; fp32 outputs [rows, D] and lse [rows], 256-aligned
+    rows = 128 * 32 * 8
+    want = ((rows * 128 * 4 + 255) // 256) * 256 + ((rows * 4 + 255) // 256) * 256
+    assert P.paged_attn_decode_workspace_size(128, 32, 8, 128, 8192, 1024) == want
+    assert P.paged_attn_decode_workspace_size(4, 8, 2, 64, 100, 256) == 256   # no split
+    assert P.paged_attn_decode_workspace_size(4, 8, 2, 64, 100, 24) == 0      # invalid
+
+
+def _prefill(lib, **kw):
+    a = dict(out=FAKE, q=FAKE, q_dtype=BF16, k=FAKE, v=FAKE, kv_dtype=BF16, bt=FAKE, sl=FAKE,
+             cu=FAKE, n=1, T=10, maxq=10, Hq=8, Hkv=2, D=128, BS=16, maxb=8, nb=64, scale=0.1,
+             ks=None, vs=None, lse=None, stream=None)
+    a.update(kw)
+    return lib.paged_attn_prefill_chunk(a["out"], a["q"], a["q_dtype"], a["k"], a["v"],
+                                        a["kv_dtype"], a["bt"], a["sl"], a["cu"], a["n"], a["T"],
+                                        a["maxq"], a["Hq"], a["Hkv"], a["D"], a["BS"], a["maxb"],
+                                        a["nb"], a["scale"], a["ks"], a["vs"], a["lse"],
+                                        a["stream"])
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(D=256), UNSUPPORTED), (dict(cu=None), INVALID), (dict(kv_dtype=FP8), INVALID),
+    (dict(BS=1), UNSUPPORTED), (dict(T=0, out=None), OK), (dict(Hq=7, Hkv=2), INVALID),
+])
+def test_prefill_argument_checks(lib, kw, want):
+    assert _prefill(lib, **kw) == want
+
+
+def _cache(lib, **kw):
+    a = dict(k=FAKE, v=FAKE, src=BF16, kc=FAKE, vc=FAKE, kv=FP8, slots=FAKE, T=4, Hkv=2, D=128,
+             BS=16, nb=8, ks=FAKE, vs=FAKE, stream=None)
+    a.update(kw)
+    return lib.reshape_and_cache(a["k"], a["v"], a["src"], a["kc"], a["vc"], a["kv"], a["slots"],
+                                 a["T"], a["Hkv"], a["D"], a["BS"], a["nb"], a["ks"], a["vs"],
+                                 a["stream"])
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(ks=None), INVALID), (dict(src=FP8), UNSUPPORTED), (dict(D=80), UNSUPPORTED),
+    (dict(slots=None), INVALID), (dict(T=0, k=None), OK), (dict(kc=FAKE + 4), INVALID),
+    (dict(src=F16, kv=BF16), UNSUPPORTED),
+])
+def test_cache_write_argument_checks(lib, kw, want):
+    assert _cache(lib, **kw) == want

@@ -1,0 +1,297 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the
+same seeded inputs. Cache writes are compared byte for byte; attention
+outputs within the stated max-abs tolerances."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_decode_11_gb300 as P
+from oracle import oracle as O
+from workloads import make_case, empty_cache
+from tests.gpu_helpers import (LSE_TOL, assert_close, check_device_ok, dev, oracle_cache,
+                               oracle_decode, product_cache, run_decode, run_prefill, scales,
+                               tol)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from paged_kv_decode_11_gb300 import build
+    build.build()
+    P.load()
+    O.build()
+    torch.cuda.init()
+    P.pkv_get_device_error()          # start from a clear error word
+
+
+# ---- reshape_and_cache: bit exact ------------------------------------------
+
+@pytest.mark.parametrize("dtype,kv,D", [("f16", "same", 64), ("bf16", "same", 128),
+                                        ("bf16", "fp8", 128), ("f16", "fp8", 64),
+                                        ("bf16", "fp8", 64)])
+def test_reshape_and_cache_bit_exact(dtype, kv, D):
+    c = make_case("tiny", 1, dtype=dtype, kv=kv, D=D, ctx=("fixed", [1, 16, 17, 255]))
+    kc, vc = product_cache(c)
+    ko, vo = oracle_cache(c)
+    check_device_ok()
+    for g, o in ((kc, ko), (vc, vo)):
+        gb = g.cpu().view(torch.uint8).numpy()
+        ob = o.view(torch.uint8).numpy()
+        assert np.array_equal(gb, ob), f"{(gb != ob).sum()} bytes differ"
+
+
+def test_reshape_and_cache_skips_negative_slots_and_flags_bad_ones():
+    c = make_case("tiny", 2, kv="fp8", dtype="bf16", D=128)
+    kc, vc = empty_cache(c, "cuda")
+    before = kc.clone()
+    ks, vs = scales(c)
+    slots = torch.tensor([-1, -5, c.num_blocks * 16, c.num_blocks * 16 + 3], dtype=torch.int64)
+    k = dev(c.new_k[:4])
+    P.reshape_and_cache(k, k, kc, vc, dev(slots), ks, vs)
+    bits = P.pkv_get_device_error()
+    assert bits == 0x2
+    assert torch.equal(kc, before)
+
+
+def test_fp8_encode_edge_values_bit_exact():
+    # saturation, ties, subnormals, signed zero: every E4M3 code value, the
+    # midpoints between neighbours, and values beyond +-448
+    codes = torch.arange(0, 256, dtype=torch.int32)
+    vals = np.array([O.e4m3_value(int(x)) for x in codes])
+    fin = np.sort(np.unique(vals[np.isfinite(vals)]))
+    mids = (fin[1:] + fin[:-1]) / 2
+    extra = np.array([449.0, 464.0, 500.0, 1e6, -1e6, 2.0 ** -11, -2.0 ** -11, 2.0 ** -10,
+                      -0.0, 0.0, 3.0e-8])
+    x = np.concatenate([fin, mids, extra]).astype(np.float32)
+    D, Hkv = 64, 1
+    T = -(-len(x) // D)
+    xs = np.zeros(T * D, np.float32)
+    xs[:len(x)] = x
+    # the values pass through bf16 sources exactly only if representable; use
+    # f16, which holds every E4M3 value and midpoint in range
+    src = torch.from_numpy(xs).to(torch.float16).view(T, Hkv, D)
+    nb = -(-T // 16) + 1
+    kc = torch.zeros((nb, Hkv, 16, D), dtype=torch.uint8)
+    vc = kc.clone()
+    ks = np.array([1.0], np.float32)
+    slots = np.arange(T, dtype=np.int64)
+    O.reshape_and_cache(src, src, kc, vc, slots, ks, ks)
+    kg = torch.zeros_like(kc).cuda()
+    vg = torch.zeros_like(kg)
+    P.reshape_and_cache(dev(src), dev(src), kg, vg, dev(slots), dev(ks), dev(ks))
+    check_device_ok()
+    assert torch.equal(kg.cpu(), kc)
+
+
+# ---- decode -------------------------------------------------------------------
+
+def _decode_vs_oracle(c, partition_tokens=None, sel=None):
+    kc, vc = product_cache(c)
+    out, lse = run_decode(c, kc, vc, partition_tokens=partition_tokens)
+    check_device_ok()
+    ko, vo = oracle_cache(c, seqs=sel)
+    want, wlse = oracle_decode(c, ko, vo, sel=sel)
+    idx = slice(None) if sel is None else torch.as_tensor(sel)
+    e = assert_close(out[idx], want, tol(c), f"{c.name} out")
+    assert_close(lse[idx], wlse, LSE_TOL, f"{c.name} lse")
+    return e
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_decode_tiny(seed):
+    _decode_vs_oracle(make_case("tiny", seed))
+
+
+@pytest.mark.parametrize("part", [16, 48, 64, 256])
+@pytest.mark.parametrize("kv", ["same", "fp8"])
+def test_decode_forced_partitions(part, kv):
+    c = make_case("tiny", 3, kv=kv, ctx=("fixed", [17, 64, 100, 700]), pool=("blocks", 128))
+    _decode_vs_oracle(c, partition_tokens=part)
+
+
+SHAPES = [
+    # (D, Hq, Hkv, dtype, kv)
+    (64, 8, 2, "f16", "same"), (128, 8, 8, "bf16", "same"), (128, 28, 4, "bf16", "same"),
+    (128, 32, 8, "bf16", "fp8"), (128, 16, 1, "f16", "fp8"), (64, 16, 2, "bf16", "fp8"),
+    (128, 32, 2, "f16", "same"), (64, 12, 12, "bf16", "same"), (128, 14, 2, "bf16", "fp8"),
+]
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,dtype,kv", SHAPES)
+@pytest.mark.parametrize("part", [0, 32])
+def test_decode_shape_sweep(D, Hq, Hkv, dtype, kv, part):
+    ctx = [1, 15, 16, 17, 31, 33, 130, 300]
+    c = make_case("tiny", 4, B=len(ctx), Hq=Hq, Hkv=Hkv, D=D, dtype=dtype, kv=kv,
+                  ctx=("fixed", ctx), pool=("scale", 1.5))
+    _decode_vs_oracle(c, partition_tokens=part)
+
+
+def test_decode_empty_sequences():
+    c = make_case("tiny", 5, ctx=("fixed", [0, 40, 0, 1]))
+    kc, vc = product_cache(c)
+    out, lse = run_decode(c, kc, vc, partition_tokens=16)
+    check_device_ok()
+    for b in (0, 2):
+        assert torch.all(out[b] == 0) and torch.all(torch.isneginf(lse[b]))
+    ko, vo = oracle_cache(c)
+    want, wlse = oracle_decode(c, ko, vo)
+    assert_close(out, want, tol(c), "out")
+
+
+@pytest.mark.parametrize("kv", ["same", "fp8"])
+def test_decode_length_one_is_v_row_bit_exact(kv):
+    c = make_case("tiny", 6, ctx=("fixed", [1, 1, 1, 1]), kv=kv)
+    kc, vc = product_cache(c)
+    out, _ = run_decode(c, kc, vc)
+    ko, vo = oracle_cache(c)
+    want, _ = oracle_decode(c, ko, vo)
+    # one token: p = 1 exactly, so out is the (dequantised) V row, rounded once
+    ref = torch.from_numpy(want).to(c.torch_dtype)
+    assert torch.equal(out.cpu(), ref)
+
+
+def test_decode_block_permutation_and_shared_prefix_bit_identical():
+    cfg = dict(B=6, Hq=8, Hkv=2, D=128, BS=16, dtype="bf16", kv="same",
+               ctx=("uniform", 40, 400), pool=("scale", 2.0), partition_tokens=0,
+               shared_prefix=(3, 32), prefill=None)
+    c = make_case(cfg, 7)
+    kc, vc = product_cache(c)
+    out, lse = run_decode(c, kc, vc, partition_tokens=64)
+    perm = torch.from_numpy(np.random.default_rng(3).permutation(c.num_blocks)).cuda()
+    k2, v2 = torch.empty_like(kc), torch.empty_like(vc)
+    k2[perm], v2[perm] = kc, vc
+    t2 = perm.cpu().numpy()[c.block_tables].astype(np.int32)
+    out2, lse2 = run_decode(c, k2, v2, partition_tokens=64, block_tables=t2)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    # private copies of the shared prefix blocks
+    used = set(c.block_tables.ravel().tolist())
+    free = [i for i in range(c.num_blocks) if i not in used]
+    t3 = c.block_tables.copy()
+    k3, v3 = kc.clone(), vc.clone()
+    for b in (1, 2):
+        for i in range(2):
+            nid = free.pop()
+            k3[nid], v3[nid] = kc[t3[b, i]], vc[t3[b, i]]
+            t3[b, i] = nid
+    out3, lse3 = run_decode(c, k3, v3, partition_tokens=64, block_tables=t3)
+    check_device_ok()
+    assert torch.equal(out, out3) and torch.equal(lse, lse3)
+
+
+def test_decode_flags_bad_block_id_and_seq_len():
+    c = make_case("tiny", 8)
+    kc, vc = product_cache(c)
+    bt = c.block_tables.copy()
+    bt[1, 0] = c.num_blocks + 5
+    run_decode(c, kc, vc, block_tables=bt)
+    assert P.pkv_get_device_error() & 0x1
+    sl = c.seq_lens.copy()
+    sl[2] = c.max_seq_len + 40
+    run_decode(c, kc, vc, seq_lens=sl)
+    assert P.pkv_get_device_error() & 0x4
+
+
+def test_decode_rejects_missing_workspace():
+    c = make_case("tiny", 0)
+    kc, vc = product_cache(c)
+    q = dev(c.q)
+    with pytest.raises(P.PkvError) as ei:
+        P.paged_attn_decode(torch.empty_like(q), q, kc, vc, dev(c.block_tables),
+                            dev(c.seq_lens), float(c.scale), c.max_seq_len, partition_tokens=16,
+                            workspace=torch.empty(16, dtype=torch.uint8, device="cuda"))
+    assert ei.value.status == 3
+
+
+# ---- full-size workloads, sampled outputs ----------------------------------------
+
+@pytest.mark.parametrize("name,sel", [("qwen2.5-7b", [0, 5, 17, 31]),
+                                      ("llama3-8b-fp8", [0, 9, 64, 127]),
+                                      ("long-ctx", [0, 3])])
+def test_decode_full_size_sampled(name, sel):
+    c = make_case(name, 0, device="cuda")
+    # the launch configuration the bench times (automatic partitions unless
+    # the workload fixes them)
+    _decode_vs_oracle(c, sel=sel)
+
+
+# ---- prefill -------------------------------------------------------------------
+
+def _prefill_case(seed, L, P_, dtype="f16", kv="same", Hq=4, Hkv=2, D=64):
+    cfg = dict(B=2, Hq=Hq, Hkv=Hkv, D=D, BS=16, dtype=dtype, kv=kv, ctx=("fixed", [20, 33]),
+               pool=("scale", 2.0), partition_tokens=0, shared_prefix=None, prefill=(L, P_))
+    return make_case(cfg, seed)
+
+
+@pytest.mark.parametrize("L,P_,dtype,kv,Hq,Hkv,D", [
+    (1, 40, "f16", "same", 4, 2, 64), (37, 0, "f16", "same", 4, 2, 64),
+    (50, 29, "bf16", "same", 8, 2, 128), (23, 17, "bf16", "fp8", 8, 2, 128),
+    (100, 300, "bf16", "same", 16, 8, 128), (65, 7, "f16", "fp8", 14, 2, 64),
+    (129, 130, "bf16", "same", 7, 7, 128)])
+def test_prefill_vs_oracle(L, P_, dtype, kv, Hq, Hkv, D):
+    c = _prefill_case(9, L, P_, dtype, kv, Hq, Hkv, D)
+    kc, vc = product_cache(c)
+    out, lse = run_prefill(c, kc, vc)
+    check_device_ok()
+    ko, vo = oracle_cache(c)
+    pf = c.prefill
+    want, wlse = O.prefill_chunk(pf.q, ko, vo, pf.block_tables, pf.seq_lens, pf.cu_q_lens,
+                                 c.scale, c.k_scales, c.v_scales)
+    assert_close(out, want, tol(c), "prefill out")
+    assert_close(lse, wlse, LSE_TOL, "prefill lse")
+
+
+def test_prefill_several_sequences_in_one_call():
+    # three sequences with different chunk lengths and histories
+    c = _prefill_case(10, 10, 10, "bf16", "same", 8, 2, 128)
+    kc, vc = product_cache(c)
+    ko, vo = oracle_cache(c)
+    # reuse the two decode sequences as extra prefill sequences: their chunk
+    # is their last few tokens
+    tables = np.zeros((3, max(c.block_tables.shape[1], c.prefill.block_tables.shape[1])), np.int32)
+    tables[:2, :c.block_tables.shape[1]] = c.block_tables
+    tables[2, :c.prefill.block_tables.shape[1]] = c.prefill.block_tables[0]
+    seq_lens = np.array([c.seq_lens[0], c.seq_lens[1], c.prefill.seq_lens[0]], np.int32)
+    Ls = [5, 33, 10]
+    cu = np.array([0, 5, 38, 48], np.int32)
+    g = torch.Generator().manual_seed(4)
+    q = torch.randn((48, c.Hq, c.D), generator=g).to(torch.bfloat16)
+    out = torch.empty_like(q).cuda()
+    P.paged_attn_prefill_chunk(out, dev(q), kc, vc, dev(tables), dev(seq_lens), dev(cu),
+                               float(c.scale), max(Ls))
+    check_device_ok()
+    want, _ = O.prefill_chunk(q, ko, vo, tables, seq_lens, cu, c.scale)
+    assert_close(out, want, 1e-2, "multi-seq prefill")
+
+
+def test_prefill_flags_chunk_longer_than_context():
+    c = _prefill_case(11, 8, 4)
+    kc, vc = product_cache(c)
+    pf = c.prefill
+    q = dev(pf.q)
+    out = torch.zeros_like(q)
+    P.paged_attn_prefill_chunk(out, q, kc, vc, dev(pf.block_tables), dev(np.array([5], np.int32)),
+                               dev(pf.cu_q_lens), float(c.scale), pf.L)
+    assert P.pkv_get_device_error() & 0x10
+
+
+# ---- the mixed continuous-batching step ----------------------------------------------
+
+def test_mixed_step_vs_oracle():
+    from paged_kv_decode_11_gb300.step import MixedStep
+    c = make_case("mixed", 0, device="cuda")
+    kc, vc = product_cache(c, write_new=False)
+    step = MixedStep.from_case(c, kc, vc)
+    step.run()
+    torch.cuda.synchronize()
+    check_device_ok()
+    sel = [0, 7, 15, 16, 40, 63]                       # 0..15 share the prefix
+    ko, vo = oracle_cache(c)
+    want, wlse = oracle_decode(c, ko, vo, sel=sel)
+    assert_close(step.out[torch.as_tensor(sel)], want, tol(c), "mixed decode")
+    pf = c.prefill
+    pw, _ = O.prefill_chunk(pf.q.cpu(), ko, vo, pf.block_tables, pf.seq_lens, pf.cu_q_lens,
+                            c.scale)
+    assert_close(step.prefill_out, pw, tol(c), "mixed prefill")
+    # the step wrote the same cache bytes as the oracle
+    assert torch.equal(kc.cpu().view(torch.uint8), ko.view(torch.uint8))

@@ -2,8 +2,8 @@
 
 This module is shared by the CUDA path's callers (tests, bench) and by the
 oracle's tests. It draws numbers and lays out the paged pool; it holds none of
-the attention arithmetic and none of the cache-write arithmetic (the FP8
-encode lives on each side separately).
+the attention arithmetic and none of the cache-write arithmetic (each side
+quantises to FP8 with its own code).
 
 Recipe (all draws seeded):
   * metadata (context lengths, block placement) from numpy's PCG64
