@@ -83,11 +83,12 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
 
 /*
  * paged_attn_decode_workspace_size
- *   Bytes of device workspace paged_attn_decode needs for these sizes
- *   (fp32 partial outputs and log-sum-exps of the split-KV partitions).
- *   partition_tokens: as passed to paged_attn_decode (0 = automatic; the
- *   automatic choice depends on the current device's SM count, so query on
- *   the device that will run the call). Returns 0 for invalid sizes.
+ *   Bytes of device workspace paged_attn_decode needs for these sizes: the
+ *   per-(sequence, KV head) partition counters and the fp32 partial outputs
+ *   and log-sum-exps of the split-KV partitions. partition_tokens: as passed
+ *   to paged_attn_decode (0 = automatic; the automatic size depends on the
+ *   current device's SM count, so query on the device that will run the
+ *   call). Returns 0 for invalid sizes.
  */
 size_t paged_attn_decode_workspace_size(int num_seqs, int num_q_heads,
                                         int num_kv_heads, int head_dim,
@@ -100,16 +101,21 @@ size_t paged_attn_decode_workspace_size(int num_seqs, int num_q_heads,
  *     out   = v_scale[g] * sum_j softmax(s)_j * Vcode_j          (q dtype, RNE)
  *     lse   = log(sum_j exp(s_j))                                (natural log)
  *   (k_scale = v_scale = 1 unless kv_dtype is FP8_E4M3.)
- *   The context is cut into partitions of `partition_tokens` tokens
- *   (multiple of 16, or 0 = automatic); each partition is reduced with an
- *   online softmax and the partitions are merged by log-sum-exp.
+ *   Each context is cut into partitions (of `partition_tokens` tokens, a
+ *   multiple of 16 up to 8192, or 0 = automatic sizes); each partition is
+ *   reduced with an online softmax and the partitions of a sequence are
+ *   merged by log-sum-exp in the same kernel launch.
  *   seq_lens[b] == 0 gives out = 0 and lse = -inf.
- *   max_seq_len: upper bound on every seq_lens[b] (sizes the grid); a larger
+ *   max_seq_len: upper bound on every seq_lens[b] (sizes the plan); a larger
  *   seq_len sets PKV_DEVERR_SEQ_LEN and is clamped.
  *   k_scales, v_scales: fp32 [Hkv], required for FP8 KV, ignored otherwise.
  *   out_lse: optional fp32 [B, Hq] (NULL to skip).
- *   workspace: device buffer of at least paged_attn_decode_workspace_size()
- *   bytes; its contents need no initialisation and are clobbered.
+ *   workspace: 256-byte aligned device buffer of at least
+ *   paged_attn_decode_workspace_size() bytes, always required. Its contents
+ *   need no initialisation: when contexts may span several partitions the
+ *   call enqueues a clear of its counter region (cudaMemsetAsync on
+ *   `stream`) before the kernel. Two calls that share a workspace must not
+ *   overlap on the GPU.
  */
 pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype,
                              const void* k_cache, const void* v_cache,

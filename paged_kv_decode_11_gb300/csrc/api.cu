@@ -4,6 +4,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+#include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -99,20 +101,36 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Automatic split-KV partition size: enough (partition, KV head, sequence)
-// CTAs for about 16 per SM when the contexts average half the maximum,
-// between 256 and 1024 tokens (a power of two).
-int auto_partition(int num_seqs, int num_kv_heads, int max_seq_len, int sms) {
-  const int64_t est = (int64_t)num_seqs * num_kv_heads * (max_seq_len / 2 + 1);
-  const int64_t target = (int64_t)(sms > 0 ? sms : 148) * 16;
-  int part = 256;
-  while (part < 1024 && est / part > target) part *= 2;
-  return part;
-}
+// Split-KV plan of a decode call: contexts are cut into partitions of
+// `part` tokens (one CTA each). The automatic size is the smallest power of
+// two from 256 to 2048 tokens that keeps the launch at about 8 waves of
+// resident CTAs when contexts average half the maximum (fewer, larger
+// partitions cost less per CTA; enough of them keep every SM busy).
+// Workspace: [done counters B*Hkv u64 | partition outputs B*Hq*max_parts*D
+// fp32 | partition log2-sum-exps B*Hq*max_parts fp32], each region 256-byte
+// aligned.
+struct DecodePlan {
+  int part, max_parts;
+  size_t off_o, off_lse, bytes;
+};
 
-int plan_partition(int num_seqs, int num_kv_heads, int max_seq_len, int partition_tokens) {
-  if (partition_tokens > 0) return partition_tokens;
-  return auto_partition(num_seqs, num_kv_heads, max_seq_len, sm_count());
+DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                       int max_seq_len, int partition_tokens, int sms) {
+  DecodePlan pl{};
+  if (partition_tokens > 0) {
+    pl.part = partition_tokens;
+  } else {
+    const int64_t est = (int64_t)num_seqs * num_kv_heads * std::max(1, max_seq_len / 2);
+    const int64_t target = (int64_t)(sms > 0 ? sms : 148) * kDecodeWorkers * 8;
+    pl.part = 256;
+    while (pl.part < 2048 && est / pl.part > target) pl.part *= 2;
+  }
+  pl.max_parts = std::max(1, (max_seq_len + pl.part - 1) / pl.part);
+  const size_t rows = (size_t)num_seqs * num_q_heads * pl.max_parts;
+  pl.off_o = align256((size_t)num_seqs * num_kv_heads * 8);
+  pl.off_lse = pl.off_o + align256(rows * head_dim * sizeof(float));
+  pl.bytes = pl.off_lse + align256(rows * sizeof(float));
+  return pl;
 }
 
 bool valid_dtypes(pkv_dtype q, pkv_dtype kv) {
@@ -133,11 +151,9 @@ size_t paged_attn_decode_workspace_size(int num_seqs, int num_q_heads, int num_k
       max_seq_len < 0 || partition_tokens < 0 || partition_tokens % 16 != 0 ||
       partition_tokens > kMaxPartitionTokens)
     return 0;
-  const int part = plan_partition(num_seqs, num_kv_heads, max_seq_len, partition_tokens);
-  const int64_t max_parts = max_seq_len > 0 ? (max_seq_len + part - 1) / part : 1;
-  if (max_parts <= 1) return 256;
-  const size_t rows = (size_t)num_seqs * num_q_heads * max_parts;
-  return align256(rows * head_dim * sizeof(float)) + align256(rows * sizeof(float));
+  return plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                     partition_tokens, sm_count())
+      .bytes;
 }
 
 pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const void* k_cache,
@@ -167,24 +183,24 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const 
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_ERR_INVALID_ARG;
 
-  const int part = plan_partition(num_seqs, num_kv_heads, max_seq_len, partition_tokens);
-  const int max_parts = max_seq_len > 0 ? (max_seq_len + part - 1) / part : 1;
-  DecodeParams p{};
-  if (max_parts > 1) {
-    const size_t rows = (size_t)num_seqs * num_q_heads * max_parts;
-    const size_t o_bytes = align256(rows * head_dim * sizeof(float));
-    const size_t need = o_bytes + align256(rows * sizeof(float));
-    if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
-      return PKV_ERR_WORKSPACE;
-    p.ws_o = static_cast<float*>(workspace);
-    p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
-  }
+  const int sms = sm_count();
+  const DecodePlan pl = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                                    partition_tokens, sms);
+  if (workspace == nullptr || workspace_bytes < pl.bytes ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return PKV_ERR_WORKSPACE;
   CUtensorMap tmK, tmV;
   if (!make_kv_tmap(&tmK, k_cache, kv_dtype, head_dim, num_kv_heads, num_blocks) ||
       !make_kv_tmap(&tmV, v_cache, kv_dtype, head_dim, num_kv_heads, num_blocks))
     return PKV_ERR_CUDA;
   unsigned int* err = err_word();
   if (err == nullptr) return PKV_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  // the partition counters start from zero in every call
+  if (pl.max_parts > 1 &&
+      cudaMemsetAsync(ws, 0, pl.off_o, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PKV_ERR_CUDA;
+  DecodeParams p{};
   p.out = out;
   p.q = q;
   p.block_tables = block_tables;
@@ -192,6 +208,9 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const 
   p.k_scales = k_scales;
   p.v_scales = v_scales;
   p.out_lse = out_lse;
+  p.done = reinterpret_cast<unsigned long long*>(ws);
+  p.ws_o = reinterpret_cast<float*>(ws + pl.off_o);
+  p.ws_lse = reinterpret_cast<float*>(ws + pl.off_lse);
   p.err = err;
   p.B = num_seqs;
   p.Hq = num_q_heads;
@@ -200,8 +219,8 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const 
   p.max_blocks = max_blocks_per_seq;
   p.num_blocks = num_blocks;
   p.max_seq_len = max_seq_len;
-  p.part = part;
-  p.max_parts = max_parts;
+  p.part = pl.part;
+  p.max_parts = pl.max_parts;
   p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   return launch_decode(p, head_dim, q_dtype, kv_dtype, tmK, tmV,
                        reinterpret_cast<cudaStream_t>(stream));

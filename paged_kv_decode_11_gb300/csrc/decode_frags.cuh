@@ -1,0 +1,212 @@
+// decode_frags.cuh — page products of the decode kernel with the query heads
+// in the MMA N dimension.
+//
+// With one query token per sequence, a GQA group has G <= 16 query rows; as
+// the M dimension of m16n8k16 they would leave most of the tile empty. The
+// decode products are therefore transposed, so the heads fill N (8 per
+// n-tile, NT = 1 for G <= 8, 2 for G <= 16):
+//   S^T[16 tokens x 8NT heads]  = K_page[16 x D] . Q^T[D x 8NT]   (D/16 k-steps)
+//   O^T[D x 8NT]               += V_page^T[D x 16] . P^T[16 x 8NT] (D/16 m-tiles)
+// P^T is built from the S^T accumulators with movmatrix (an in-register 8x8
+// transpose), so no shared memory round trip is needed. Accumulator state
+// per thread: O^T NT x D/16 x 4 fp32, Q^T NT x D/16 x 2 registers.
+//
+// E4M3 caches: the K operand is the A fragment. The contraction index d is
+// permuted (thread with c = lane%4 takes chunk 4u + c of its token row;
+// byte pair (4i, 4i+1) of that chunk feeds a0/a1 and (4i+2, 4i+3) feeds a2/a3
+// of k-step 4u + i), and the Q^T fragments follow the same permutation.
+// Tokens: accumulator row r (0..7) is token pi(r) = r ^ ((r & 1) << 2), and
+// row r + 8 is token 8 + pi(r); with the 128-byte swizzle this keeps every
+// 8-lane phase of the 16-byte K and V reads on distinct banks. The V^T
+// operand takes thread g = lane/4's D/8 contiguous bytes of four token rows
+// and interleaves token pairs with byte permutes; m-tile t, row g is dim
+// (D/8) g + 2t and row g + 8 is dim (D/8) g + 2t + 1.
+#pragma once
+#include "common.cuh"
+
+namespace pkv {
+
+// Token (0..15) of S^T accumulator row g (r8 = 0) or g + 8 (r8 = 1).
+template <int KV>
+__device__ __forceinline__ int st_row_token(int g, int r8) {
+  if constexpr (KV == KV_E4M3) return 8 * r8 + (g ^ ((g & 1) << 2));
+  else return 8 * r8 + g;
+}
+
+// Head dimension of O^T accumulator row g (r8 = 0) or g + 8 (r8 = 1) of m-tile t.
+template <int D, int KV>
+__device__ __forceinline__ int ot_row_dim(int t, int g, int r8) {
+  if constexpr (KV == KV_E4M3) return (D / 8) * g + 2 * t + r8;
+  else return 16 * t + g + 8 * r8;
+}
+
+// Q^T fragments (B operand, D x 8NT) from the G query rows [G][D] of a GQA
+// group in shared memory; head columns >= G are zero. 16-bit q, converted to
+// f16 for E4M3 caches.
+template <int D, int KV, bool QBF16, int NT>
+__device__ __forceinline__ void load_qT_frags(uint32_t (&qf)[NT][D / 16][2],
+                                              const uint16_t* qs, int G, int lane) {
+  const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const bool live = 8 * nt + g < G;
+    const uint16_t* row = qs + (live ? (8 * nt + g) : 0) * D;
+#pragma unroll
+    for (int s = 0; s < D / 16; ++s) {
+      int d0, d1;
+      if constexpr (KV == KV_E4M3) {
+        const int u = s >> 2, i = s & 3;
+        d0 = 16 * (4 * u + c) + 4 * i;
+        d1 = d0 + 2;
+      } else {
+        d0 = 16 * s + 2 * c;
+        d1 = d0 + 8;
+      }
+      uint32_t r0 = *reinterpret_cast<const uint32_t*>(row + d0);
+      uint32_t r1 = *reinterpret_cast<const uint32_t*>(row + d1);
+      if constexpr (KV == KV_E4M3 && QBF16) {
+        float2 f0 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&r0));
+        float2 f1 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&r1));
+        r0 = pack_f16x2(f0.x, f0.y);
+        r1 = pack_f16x2(f1.x, f1.y);
+      }
+      qf[nt][s][0] = live ? r0 : 0u;
+      qf[nt][s][1] = live ? r1 : 0u;
+    }
+  }
+}
+
+// acc[nt][.] += K_page . Q^T for the page at shared-memory byte address kpage.
+template <int D, int KV, int NT>
+__device__ __forceinline__ void kq_page(float (&acc)[NT][4], const uint32_t (&qf)[NT][D / 16][2],
+                                        uint32_t kpage, int lane) {
+  using Geo = PageGeom<D, KV>;
+  if constexpr (KV == KV_E4M3) {
+    const int g = lane >> 2, c = lane & 3;
+    const int t0 = g ^ ((g & 1) << 2);
+#pragma unroll
+    for (int u = 0; u < D / 64; ++u) {
+      const uint4 w0 = lds128(kpage + Geo::swz(t0, 16 * (4 * u + c)));
+      const uint4 w1 = lds128(kpage + Geo::swz(8 + t0, 16 * (4 * u + c)));
+      const uint32_t lo[4] = {w0.x, w0.y, w0.z, w0.w};
+      const uint32_t hi[4] = {w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        uint32_t a[4];
+        a[0] = e4m3x2_to_f16x2(lo[i] & 0xFFFFu);
+        a[1] = e4m3x2_to_f16x2(hi[i] & 0xFFFFu);
+        a[2] = e4m3x2_to_f16x2(lo[i] >> 16);
+        a[3] = e4m3x2_to_f16x2(hi[i] >> 16);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+          mma_f16(acc[nt], a, qf[nt][4 * u + i][0], qf[nt][4 * u + i][1]);
+      }
+    }
+  } else {
+    constexpr bool BF = (KV == KV_BF16);
+    const int mi = lane >> 3, r = lane & 7;
+    const int tok = r + 8 * (mi & 1);
+#pragma unroll
+    for (int s = 0; s < D / 16; ++s) {
+      uint32_t a[4];
+      ldmatrix_x4(a, kpage + Geo::elem_off(tok, 16 * s + 8 * (mi >> 1)));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma16816<BF>(acc[nt], a, qf[nt][s][0], qf[nt][s][1]);
+    }
+  }
+}
+
+// P^T B fragments from the probabilities held in S^T accumulator layout:
+// p[nt][0..1] = tokens of row g, heads 2c, 2c+1; p[nt][2..3] = row g + 8.
+template <int KV, int NT>
+__device__ __forceinline__ void pT_frags(uint32_t (&pb)[NT][2], const float (&p)[NT][4]) {
+  constexpr bool BF = (KV == KV_BF16);
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    pb[nt][0] = movmatrix_trans(pack2<BF>(p[nt][0], p[nt][1]));
+    pb[nt][1] = movmatrix_trans(pack2<BF>(p[nt][2], p[nt][3]));
+  }
+}
+
+// oacc[nt][t][.] += V_page^T . P^T for the page at shared-memory byte address vpage.
+template <int D, int KV, int NT>
+__device__ __forceinline__ void vp_page(float (&oacc)[NT][D / 16][4], const uint32_t (&pb)[NT][2],
+                                        uint32_t vpage, int lane) {
+  using Geo = PageGeom<D, KV>;
+  if constexpr (KV == KV_E4M3) {
+    const int g = lane >> 2, c = lane & 3;
+    const int ta = 2 * c, tb = (2 * c + 1) ^ 4;     // pi(2c), pi(2c+1)
+    constexpr int CH = D / 8;                      // bytes per token row for this thread
+    const uint32_t xo = CH * g;
+    uint32_t wa[CH / 4], wb[CH / 4], wc[CH / 4], wd[CH / 4];
+    if constexpr (CH == 16) {
+      const uint4 a = lds128(vpage + Geo::swz(ta, xo));
+      const uint4 b = lds128(vpage + Geo::swz(tb, xo));
+      const uint4 cc = lds128(vpage + Geo::swz(8 + ta, xo));
+      const uint4 d = lds128(vpage + Geo::swz(8 + tb, xo));
+      wa[0] = a.x; wa[1] = a.y; wa[2] = a.z; wa[3] = a.w;
+      wb[0] = b.x; wb[1] = b.y; wb[2] = b.z; wb[3] = b.w;
+      wc[0] = cc.x; wc[1] = cc.y; wc[2] = cc.z; wc[3] = cc.w;
+      wd[0] = d.x; wd[1] = d.y; wd[2] = d.z; wd[3] = d.w;
+    } else {
+      const uint2 a = lds64(vpage + Geo::swz(ta, xo));
+      const uint2 b = lds64(vpage + Geo::swz(tb, xo));
+      const uint2 cc = lds64(vpage + Geo::swz(8 + ta, xo));
+      const uint2 d = lds64(vpage + Geo::swz(8 + tb, xo));
+      wa[0] = a.x; wa[1] = a.y;
+      wb[0] = b.x; wb[1] = b.y;
+      wc[0] = cc.x; wc[1] = cc.y;
+      wd[0] = d.x; wd[1] = d.y;
+    }
+#pragma unroll
+    for (int i = 0; i < CH / 4; ++i) {
+      // dims (D/8) g + 4i + {0,1} -> m-tile 2i, {2,3} -> m-tile 2i+1
+      const uint32_t lo01 = __byte_perm(wa[i], wb[i], 0x5140);
+      const uint32_t lo23 = __byte_perm(wa[i], wb[i], 0x7362);
+      const uint32_t hi01 = __byte_perm(wc[i], wd[i], 0x5140);
+      const uint32_t hi23 = __byte_perm(wc[i], wd[i], 0x7362);
+      uint32_t a0[4], a1[4];
+      a0[0] = e4m3x2_to_f16x2(lo01 & 0xFFFFu);
+      a0[1] = e4m3x2_to_f16x2(lo01 >> 16);
+      a0[2] = e4m3x2_to_f16x2(hi01 & 0xFFFFu);
+      a0[3] = e4m3x2_to_f16x2(hi01 >> 16);
+      a1[0] = e4m3x2_to_f16x2(lo23 & 0xFFFFu);
+      a1[1] = e4m3x2_to_f16x2(lo23 >> 16);
+      a1[2] = e4m3x2_to_f16x2(hi23 & 0xFFFFu);
+      a1[3] = e4m3x2_to_f16x2(hi23 >> 16);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        mma_f16(oacc[nt][2 * i], a0, pb[nt][0], pb[nt][1]);
+        mma_f16(oacc[nt][2 * i + 1], a1, pb[nt][0], pb[nt][1]);
+      }
+    }
+  } else {
+    constexpr bool BF = (KV == KV_BF16);
+    const int mi = lane >> 3, r = lane & 7;
+    const int tok = r + 8 * (mi >> 1);
+#pragma unroll
+    for (int t = 0; t < D / 16; ++t) {
+      uint32_t a[4];
+      ldmatrix_x4_trans(a, vpage + Geo::elem_off(tok, 16 * t + 8 * (mi & 1)));
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma16816<BF>(oacc[nt][t], a, pb[nt][0], pb[nt][1]);
+    }
+  }
+}
+
+// Max / sum over the 8 lanes that share c = lane % 4 (the 8 token rows g).
+__device__ __forceinline__ float col_max8(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+  return v;
+}
+
+__device__ __forceinline__ float col_sum8(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 8);
+  v += __shfl_xor_sync(0xffffffffu, v, 16);
+  return v;
+}
+
+}  // namespace pkv

@@ -9,6 +9,7 @@
 namespace pkv {
 
 constexpr int kMaxPartitionTokens = 8192;   // split-KV partition cap (block ids staged in smem)
+constexpr int kDecodeWorkers = 4;           // resident decode CTAs per SM assumed by the planner
 
 struct DecodeParams {
   void* out;
@@ -18,11 +19,13 @@ struct DecodeParams {
   const float* k_scales;
   const float* v_scales;
   float* out_lse;
-  float* ws_o;          // [B, Hq, max_parts, D] fp32 partition outputs (normalised)
-  float* ws_lse;        // [B, Hq, max_parts]    fp32 partition log2-sum-exp
-  unsigned int* err;    // device error word
-  int B, Hq, Hkv, G, max_blocks, num_blocks, max_seq_len, part, max_parts;
-  float qk_scale_log2;  // scale * log2(e)
+  unsigned long long* done;   // [B * Hkv] finished-partition counters (zero at launch)
+  float* ws_o;                // [B * Hq, max_parts, D] fp32 partition outputs (normalised)
+  float* ws_lse;              // [B * Hq, max_parts]    fp32 partition log2-sum-exp
+  unsigned int* err;          // device error word
+  int B, Hq, Hkv, G, max_blocks, num_blocks, max_seq_len;
+  int part, max_parts;        // partition size (tokens) and partitions per sequence
+  float qk_scale_log2;        // scale * log2(e)
 };
 
 struct PrefillParams {
@@ -56,6 +59,8 @@ struct CacheWriteParams {
 pkv_status launch_decode(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                          pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
                          cudaStream_t stream);
+// Dynamic shared memory of one decode CTA.
+size_t decode_smem_bytes(int head_dim, pkv_dtype kv_dtype, int G);
 pkv_status launch_prefill(const PrefillParams& p, int head_dim, pkv_dtype q_dtype,
                           pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           cudaStream_t stream);

@@ -112,6 +112,8 @@ class MixedStep:
                             self.all_new_slots, d.k_scales, d.v_scales, stream=main)
         self.ev_written.record(main)
         self.side.wait_event(self.ev_written)
+        # prefill first: its CTAs take their SMs, and the persistent decode
+        # grid claims work on whatever room is left, then everywhere
         B.paged_attn_prefill_chunk(self.prefill_out, self.pf_q, d.k_cache, d.v_cache,
                                    self.pf_block_tables, self.pf_seq_lens, self.pf_cu_q_lens,
                                    d.scale, self.pf_max_q_len, d.k_scales, d.v_scales,

@@ -76,18 +76,24 @@ def test_decode_argument_checks(lib, kw, want):
 
 
 def test_decode_workspace_check(lib):
-    # 2 partitions of 64 tokens: the workspace is required
+    # the workspace (work counters + partials) is always required, 256-aligned
     assert _decode(lib, part=64, msl=128, ws=None) == WORKSPACE
     need = P.paged_attn_decode_workspace_size(4, 8, 2, 128, 128, 64)
     assert _decode(lib, part=64, msl=128, ws=FAKE, wsb=need - 1) == WORKSPACE
+    assert _decode(lib, part=64, msl=128, ws=FAKE + 16, wsb=need) == WORKSPACE
 
 
 def test_workspace_size_formula(lib):
-    # rows = B * Hq * parts; fp32 outputs [rows, D] and lse [rows], 256-aligned
+    # counters: B*Hkv 8-byte words; partials: rows = B*Hq*parts with
+    # parts = ceil(max_seq_len / partition); each region 256-aligned
+    def a256(x):
+        return (x + 255) // 256 * 256
     rows = 128 * 32 * 8
-    want = ((rows * 128 * 4 + 255) // 256) * 256 + ((rows * 4 + 255) // 256) * 256
+    want = a256(128 * 8 * 8) + a256(rows * 128 * 4) + a256(rows * 4)
     assert P.paged_attn_decode_workspace_size(128, 32, 8, 128, 8192, 1024) == want
-    assert P.paged_attn_decode_workspace_size(4, 8, 2, 64, 100, 256) == 256   # no split
+    rows = 4 * 8 * 1
+    assert P.paged_attn_decode_workspace_size(4, 8, 2, 64, 100, 256) == \
+        a256(4 * 2 * 8) + a256(rows * 64 * 4) + a256(rows * 4)
     assert P.paged_attn_decode_workspace_size(4, 8, 2, 64, 100, 24) == 0      # invalid
 
 
