@@ -129,6 +129,43 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype,
                              void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/* Size of the scratch array paged_attn_decode_noalloc uses (32 MiB). */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * paged_attn_decode_noalloc — paged_attn_decode without a caller workspace.
+ *   The source pages have no counterpart to this call; it exists for callers
+ *   that cannot allocate device memory at the point where they run
+ *   attention: an engine whose memory planner has already handed the whole
+ *   device to weights and the KV pool, a latency-critical loop that cannot
+ *   afford cudaMalloc/cudaFree (they can synchronise the device), or a plain
+ *   C host with no allocator of its own.
+ *   Same arguments, results and errors as paged_attn_decode, minus the
+ *   workspace: the split-KV scratch is one device array of
+ *   PKV_NOALLOC_SCRATCH_BYTES inside the library, held by every GPU that
+ *   loads the library until the process exits. Sizes whose
+ *   paged_attn_decode_workspace_size() exceeds PKV_NOALLOC_SCRATCH_BYTES are
+ *   rejected with PKV_ERR_WORKSPACE before anything is launched.
+ *   Nothing here allocates. The first call on a device looks up the array's
+ *   device address (cudaGetSymbolAddress); make that first call before any
+ *   stream capture. Every call on a device shares the one array and each
+ *   call clears the counters it needs, so calls that overlap on the GPU (on
+ *   different streams, or from different threads) race: serialise them.
+ */
+pkv_status paged_attn_decode_noalloc(void* out, const void* q, pkv_dtype q_dtype,
+                                     const void* k_cache, const void* v_cache,
+                                     pkv_dtype kv_dtype,
+                                     const int32_t* block_tables,
+                                     const int32_t* seq_lens, int num_seqs,
+                                     int num_q_heads, int num_kv_heads,
+                                     int head_dim, int block_size,
+                                     int max_blocks_per_seq, int num_blocks,
+                                     int max_seq_len, float scale,
+                                     const float* k_scales,
+                                     const float* v_scales,
+                                     int partition_tokens, float* out_lse,
+                                     void* stream);
+
 /*
  * paged_attn_prefill_chunk — causal attention of a chunk of new query
  * tokens of each sequence over that sequence's paged cache.

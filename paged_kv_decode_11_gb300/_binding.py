@@ -22,8 +22,9 @@ STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
 DEVERR_BITS = {0x1: "block id", 0x2: "slot", 0x4: "seq_len", 0x8: "timeout", 0x10: "chunk length"}
 
 # Every symbol include/pkv.h declares.
-EXPORTS = ("paged_attn_decode_workspace_size", "paged_attn_decode", "paged_attn_prefill_chunk",
-           "reshape_and_cache", "pkv_get_device_error", "pkv_status_string")
+EXPORTS = ("paged_attn_decode_workspace_size", "paged_attn_decode", "paged_attn_decode_noalloc",
+           "paged_attn_prefill_chunk", "reshape_and_cache", "pkv_get_device_error",
+           "pkv_status_string")
 
 _lib = None
 
@@ -52,6 +53,9 @@ def load(path: str = LIB_PATH):
     L.paged_attn_decode.restype = I
     L.paged_attn_decode.argtypes = [P, P, I, P, P, I, P, P, I, I, I, I, I, I, I, I, F, P, P, I, P,
                                     P, S, P]
+    L.paged_attn_decode_noalloc.restype = I
+    L.paged_attn_decode_noalloc.argtypes = [P, P, I, P, P, I, P, P, I, I, I, I, I, I, I, I, F, P,
+                                            P, I, P, P]
     L.paged_attn_prefill_chunk.restype = I
     L.paged_attn_prefill_chunk.argtypes = [P, P, I, P, P, I, P, P, P, I, I, I, I, I, I, I, I, I,
                                            F, P, P, P, P]
@@ -130,6 +134,30 @@ def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
         _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream))
     _check("paged_attn_decode", st)
+
+
+def paged_attn_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                              v_cache: torch.Tensor, block_tables: torch.Tensor,
+                              seq_lens: torch.Tensor, scale: float, max_seq_len: int,
+                              k_scales: Optional[torch.Tensor] = None,
+                              v_scales: Optional[torch.Tensor] = None, partition_tokens: int = 0,
+                              out_lse: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Like paged_attn_decode, for callers that cannot allocate: the split-KV
+    scratch is the library's own fixed device array (PKV_NOALLOC_SCRATCH_BYTES),
+    so no workspace is passed and nothing is allocated. Calls that overlap on
+    the GPU share that array and race."""
+    B, Hq, D = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    assert d2 == D and out.shape == q.shape and out.dtype == q.dtype
+    assert block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32
+    st = load().paged_attn_decode_noalloc(
+        _dev_ptr(out, "out"), _dev_ptr(q, "q"), dtype_code(q), _dev_ptr(k_cache, "k_cache"),
+        _dev_ptr(v_cache, "v_cache"), dtype_code(k_cache), _dev_ptr(block_tables, "block_tables"),
+        _dev_ptr(seq_lens, "seq_lens"), B, Hq, hkv, D, bs, block_tables.shape[1], nb,
+        int(max_seq_len), float(scale), _dev_ptr(k_scales, "k_scales"),
+        _dev_ptr(v_scales, "v_scales"), int(partition_tokens), _dev_ptr(out_lse, "out_lse"),
+        _stream(stream))
+    _check("paged_attn_decode_noalloc", st)
 
 
 def paged_attn_prefill_chunk(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
