@@ -152,7 +152,20 @@ __global__ void __launch_bounds__(NW * 32)
     float s[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-    kq_page<D, KV, NT>(s, qf, kpage, lane);
+    // E4M3: take the page into registers and refill the stage at once, so the
+    // next load is in flight while this page's math runs.
+    E4M3PageRegs<D> pr;
+    if constexpr (KV == KV_E4M3) {
+      load_e4m3_page<D>(pr, kpage, vpage, lane);
+      __syncwarp();
+      if (lane == 0 && k + NST < nmine) {
+        fence_proxy_async_smem();
+        issue(k + NST);
+      }
+      kq_regs<D, NT>(s, qf, pr.k);
+    } else {
+      kq_page<D, KV, NT>(s, qf, kpage, lane);
+    }
 
     const int tbase = tok0 + (warp + NW * k) * kBS;
     const bool v0 = tbase + tk0 < tok1, v8 = tbase + tk8 < tok1;
@@ -179,12 +192,15 @@ __global__ void __launch_bounds__(NW * 32)
       }
     uint32_t pb[NT][2];
     pT_frags<KV, NT>(pb, s);
-    vp_page<D, KV, NT>(oacc, pb, vpage, lane);
-
-    __syncwarp();
-    if (lane == 0 && k + NST < nmine) {
-      fence_proxy_async_smem();
-      issue(k + NST);
+    if constexpr (KV == KV_E4M3) {
+      vp_regs<D, NT>(oacc, pb, pr.v);
+    } else {
+      vp_page<D, KV, NT>(oacc, pb, vpage, lane);
+      __syncwarp();
+      if (lane == 0 && k + NST < nmine) {
+        fence_proxy_async_smem();
+        issue(k + NST);
+      }
     }
     issued = min(k + 1 + NST, nmine);
   }

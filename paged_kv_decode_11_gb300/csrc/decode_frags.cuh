@@ -76,43 +76,145 @@ __device__ __forceinline__ void load_qT_frags(uint32_t (&qf)[NT][D / 16][2],
   }
 }
 
-// acc[nt][.] += K_page . Q^T for the page at shared-memory byte address kpage.
-template <int D, int KV, int NT>
+// Byte offset of (token r, dim d) in a page whose TMA boxes (64-element
+// column blocks of 16-bit caches) sit BSTRIDE bytes apart.
+template <int D, int KV, int BSTRIDE>
+__device__ __forceinline__ uint32_t page_off(uint32_t r, uint32_t d) {
+  using Geo = PageGeom<D, KV>;
+  return (d / Geo::BOX_ELEMS) * BSTRIDE + Geo::swz(r, (d % Geo::BOX_ELEMS) * Geo::ELT);
+}
+
+// E4M3 pages staged in registers: a thread's share of the K page (rows
+// pi(g) and 8 + pi(g), chunk 4u + c) and of the V page (rows pi(2c), pi(2c+1),
+// 8 + pi(2c), 8 + pi(2c+1), bytes (D/8) g ..). Reading them out of shared
+// memory first lets the warp refill the ring stage before the math runs.
+template <int D>
+struct E4M3PageRegs {
+  uint4 k[2][D / 64];
+  uint32_t v[4][D / 32];
+};
+
+template <int D>
+__device__ __forceinline__ void load_e4m3_page(E4M3PageRegs<D>& r, uint32_t kpage, uint32_t vpage,
+                                               int lane) {
+  using Geo = PageGeom<D, KV_E4M3>;
+  const int g = lane >> 2, c = lane & 3;
+  const int t0 = g ^ ((g & 1) << 2);
+#pragma unroll
+  for (int u = 0; u < D / 64; ++u) {
+    r.k[0][u] = lds128(kpage + Geo::swz(t0, 16 * (4 * u + c)));
+    r.k[1][u] = lds128(kpage + Geo::swz(8 + t0, 16 * (4 * u + c)));
+  }
+  const int ta = 2 * c, tb = (2 * c + 1) ^ 4;
+  constexpr int CH = D / 8;
+  const uint32_t xo = CH * g;
+  const int rows[4] = {ta, tb, 8 + ta, 8 + tb};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if constexpr (CH == 16) {
+      const uint4 w = lds128(vpage + Geo::swz(rows[q], xo));
+      r.v[q][0] = w.x; r.v[q][1] = w.y; r.v[q][2] = w.z; r.v[q][3] = w.w;
+    } else {
+      const uint2 w = lds64(vpage + Geo::swz(rows[q], xo));
+      r.v[q][0] = w.x; r.v[q][1] = w.y;
+    }
+  }
+}
+
+// acc += K . Q^T from E4M3 K words (raw[row][u]); two accumulator chains.
+template <int D, int NT>
+__device__ __forceinline__ void kq_regs(float (&acc)[NT][4], const uint32_t (&qf)[NT][D / 16][2],
+                                        const uint4 (&raw)[2][D / 64]) {
+  float acc2[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) acc2[nt][0] = acc2[nt][1] = acc2[nt][2] = acc2[nt][3] = 0.f;
+#pragma unroll
+  for (int u = 0; u < D / 64; ++u) {
+    const uint32_t lo[4] = {raw[0][u].x, raw[0][u].y, raw[0][u].z, raw[0][u].w};
+    const uint32_t hi[4] = {raw[1][u].x, raw[1][u].y, raw[1][u].z, raw[1][u].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t a[4];
+      a[0] = e4m3x2_to_f16x2(lo[i] & 0xFFFFu);
+      a[1] = e4m3x2_to_f16x2(hi[i] & 0xFFFFu);
+      a[2] = e4m3x2_to_f16x2(lo[i] >> 16);
+      a[3] = e4m3x2_to_f16x2(hi[i] >> 16);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        mma_f16((i & 1) ? acc2[nt] : acc[nt], a, qf[nt][4 * u + i][0], qf[nt][4 * u + i][1]);
+    }
+  }
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[nt][i] += acc2[nt][i];
+}
+
+// oacc += V^T . P^T from E4M3 V words (rows pi(2c), pi(2c+1), 8+.., 8+..).
+template <int D, int NT>
+__device__ __forceinline__ void vp_regs(float (&oacc)[NT][D / 16][4], const uint32_t (&pb)[NT][2],
+                                        const uint32_t (&v)[4][D / 32]) {
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i) {
+    // dims (D/8) g + 4i + {0,1} -> m-tile 2i, {2,3} -> m-tile 2i+1
+    const uint32_t lo01 = __byte_perm(v[0][i], v[1][i], 0x5140);
+    const uint32_t lo23 = __byte_perm(v[0][i], v[1][i], 0x7362);
+    const uint32_t hi01 = __byte_perm(v[2][i], v[3][i], 0x5140);
+    const uint32_t hi23 = __byte_perm(v[2][i], v[3][i], 0x7362);
+    uint32_t a0[4], a1[4];
+    a0[0] = e4m3x2_to_f16x2(lo01 & 0xFFFFu);
+    a0[1] = e4m3x2_to_f16x2(lo01 >> 16);
+    a0[2] = e4m3x2_to_f16x2(hi01 & 0xFFFFu);
+    a0[3] = e4m3x2_to_f16x2(hi01 >> 16);
+    a1[0] = e4m3x2_to_f16x2(lo23 & 0xFFFFu);
+    a1[1] = e4m3x2_to_f16x2(lo23 >> 16);
+    a1[2] = e4m3x2_to_f16x2(hi23 & 0xFFFFu);
+    a1[3] = e4m3x2_to_f16x2(hi23 >> 16);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      mma_f16(oacc[nt][2 * i], a0, pb[nt][0], pb[nt][1]);
+      mma_f16(oacc[nt][2 * i + 1], a1, pb[nt][0], pb[nt][1]);
+    }
+  }
+}
+
+// acc[nt][.] += K_page . Q^T for the page at shared-memory byte address kpage
+// (box stride BSTRIDE: several heads' pages may share each box).
+template <int D, int KV, int NT, int BSTRIDE = PageGeom<D, KV>::BOX_BYTES>
 __device__ __forceinline__ void kq_page(float (&acc)[NT][4], const uint32_t (&qf)[NT][D / 16][2],
                                         uint32_t kpage, int lane) {
   using Geo = PageGeom<D, KV>;
   if constexpr (KV == KV_E4M3) {
     const int g = lane >> 2, c = lane & 3;
     const int t0 = g ^ ((g & 1) << 2);
+    uint4 raw[2][D / 64];
 #pragma unroll
     for (int u = 0; u < D / 64; ++u) {
-      const uint4 w0 = lds128(kpage + Geo::swz(t0, 16 * (4 * u + c)));
-      const uint4 w1 = lds128(kpage + Geo::swz(8 + t0, 16 * (4 * u + c)));
-      const uint32_t lo[4] = {w0.x, w0.y, w0.z, w0.w};
-      const uint32_t hi[4] = {w1.x, w1.y, w1.z, w1.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        uint32_t a[4];
-        a[0] = e4m3x2_to_f16x2(lo[i] & 0xFFFFu);
-        a[1] = e4m3x2_to_f16x2(hi[i] & 0xFFFFu);
-        a[2] = e4m3x2_to_f16x2(lo[i] >> 16);
-        a[3] = e4m3x2_to_f16x2(hi[i] >> 16);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          mma_f16(acc[nt], a, qf[nt][4 * u + i][0], qf[nt][4 * u + i][1]);
-      }
+      raw[0][u] = lds128(kpage + Geo::swz(t0, 16 * (4 * u + c)));
+      raw[1][u] = lds128(kpage + Geo::swz(8 + t0, 16 * (4 * u + c)));
     }
+    kq_regs<D, NT>(acc, qf, raw);
   } else {
     constexpr bool BF = (KV == KV_BF16);
     const int mi = lane >> 3, r = lane & 7;
     const int tok = r + 8 * (mi & 1);
+    // two independent accumulator chains (even / odd k-steps) halve the
+    // dependent MMA latency of the contraction
+    float acc2[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) acc2[nt][0] = acc2[nt][1] = acc2[nt][2] = acc2[nt][3] = 0.f;
 #pragma unroll
     for (int s = 0; s < D / 16; ++s) {
       uint32_t a[4];
-      ldmatrix_x4(a, kpage + Geo::elem_off(tok, 16 * s + 8 * (mi >> 1)));
+      ldmatrix_x4(a, kpage + page_off<D, KV, BSTRIDE>(tok, 16 * s + 8 * (mi >> 1)));
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) mma16816<BF>(acc[nt], a, qf[nt][s][0], qf[nt][s][1]);
+      for (int nt = 0; nt < NT; ++nt)
+        mma16816<BF>((s & 1) ? acc2[nt] : acc[nt], a, qf[nt][s][0], qf[nt][s][1]);
     }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[nt][i] += acc2[nt][i];
   }
 }
 
@@ -129,7 +231,7 @@ __device__ __forceinline__ void pT_frags(uint32_t (&pb)[NT][2], const float (&p)
 }
 
 // oacc[nt][t][.] += V_page^T . P^T for the page at shared-memory byte address vpage.
-template <int D, int KV, int NT>
+template <int D, int KV, int NT, int BSTRIDE = PageGeom<D, KV>::BOX_BYTES>
 __device__ __forceinline__ void vp_page(float (&oacc)[NT][D / 16][4], const uint32_t (&pb)[NT][2],
                                         uint32_t vpage, int lane) {
   using Geo = PageGeom<D, KV>;
@@ -187,7 +289,7 @@ __device__ __forceinline__ void vp_page(float (&oacc)[NT][D / 16][4], const uint
 #pragma unroll
     for (int t = 0; t < D / 16; ++t) {
       uint32_t a[4];
-      ldmatrix_x4_trans(a, vpage + Geo::elem_off(tok, 16 * t + 8 * (mi & 1)));
+      ldmatrix_x4_trans(a, vpage + page_off<D, KV, BSTRIDE>(tok, 16 * t + 8 * (mi & 1)));
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) mma16816<BF>(oacc[nt][t], a, pb[nt][0], pb[nt][1]);
     }
