@@ -103,9 +103,10 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Split-KV plan of a decode call: contexts are cut into partitions of
 // `part` tokens (one CTA each). The automatic size is the smallest power of
-// two from 256 to 2048 tokens that keeps the launch at about 8 waves of
+// two from 256 to 2048 tokens that keeps the launch at about 3 waves of
 // resident CTAs when contexts average half the maximum (fewer, larger
-// partitions cost less per CTA; enough of them keep every SM busy).
+// partitions cost less per CTA and leave fewer partials to merge; enough of
+// them keep every SM busy).
 // Workspace: [done counters B*Hkv u64 | partition outputs B*Hq*max_parts*D
 // fp32 | partition log2-sum-exps B*Hq*max_parts fp32], each region 256-byte
 // aligned.
@@ -121,7 +122,7 @@ DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head
     pl.part = partition_tokens;
   } else {
     const int64_t est = (int64_t)num_seqs * num_kv_heads * std::max(1, max_seq_len / 2);
-    const int64_t target = (int64_t)(sms > 0 ? sms : 148) * kDecodeWorkers * 8;
+    const int64_t target = (int64_t)(sms > 0 ? sms : 148) * kDecodeWorkers * 3;
     pl.part = 256;
     while (pl.part < 2048 && est / pl.part > target) pl.part *= 2;
   }

@@ -277,28 +277,75 @@ __global__ void __launch_bounds__(NW * 32)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int idx = tid; idx < G * (D / 2); idx += NW * 32) {
-    const int hh = idx / (D / 2), d = 2 * (idx % (D / 2));
-    const int64_t wrow = (row0 + hh) * p.max_parts;
-    float M = -INFINITY;
-    for (int s2 = 0; s2 < nparts; ++s2) M = fmaxf(M, ldcg_f32(p.ws_lse + wrow + s2));
-    float Z = 0.f, o0 = 0.f, o1 = 0.f;
-    if (M != -INFINITY) {
+  // The warps split the partitions; each lane owns D/32 dims of every head.
+  // Pass 1: the largest log2-sum-exp of each head.
+  constexpr int PER = D / 32;
+  float* mbuf = red_m[0];                         // [G] maxima (G <= NH)
+  for (int hh = warp; hh < G; hh += NW) {
+    const float* lse = p.ws_lse + (row0 + hh) * p.max_parts;
+    float mx = -INFINITY;
+    for (int s2 = lane; s2 < nparts; s2 += 32) mx = fmaxf(mx, ldcg_f32(lse + s2));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) mbuf[hh] = mx;
+  }
+  __syncthreads();
+  // Pass 2: weighted sums, four heads at a time, partitions round-robin over warps.
+  for (int h0 = 0; h0 < G; h0 += 4) {
+    const int nh = min(4, G - h0);
+    float acc[4][PER], z[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      z[j] = 0.f;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) acc[j][i] = 0.f;
+    }
 #pragma unroll 4
-      for (int s2 = 0; s2 < nparts; ++s2) {
-        const float ls = ldcg_f32(p.ws_lse + wrow + s2);
-        const float2 o = __ldcg(reinterpret_cast<const float2*>(p.ws_o + (wrow + s2) * D + d));
-        const float w = (ls == -INFINITY) ? 0.f : exp2f(ls - M);
-        Z += w;
-        o0 += w * o.x;
-        o1 += w * o.y;
+    for (int s2 = warp; s2 < nparts; s2 += NW) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (j >= nh) continue;
+        const int64_t wrow = (row0 + h0 + j) * p.max_parts + s2;
+        const float M = mbuf[h0 + j];
+        const float ls = ldcg_f32(p.ws_lse + wrow);
+        const float w = (ls == -INFINITY || M == -INFINITY) ? 0.f : exp2f(ls - M);
+        z[j] += w;
+        const float* o = p.ws_o + wrow * D + lane * PER;
+        if constexpr (PER == 4) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(o));
+          acc[j][0] += w * v.x; acc[j][1] += w * v.y; acc[j][2] += w * v.z; acc[j][3] += w * v.w;
+        } else {
+          const float2 v = __ldcg(reinterpret_cast<const float2*>(o));
+          acc[j][0] += w * v.x; acc[j][1] += w * v.y;
+        }
       }
     }
-    const float inv = Z > 0.f ? vscale / Z : 0.f;
-    *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + (row0 + hh) * D + d) =
-        pack2<QBF16>(o0 * inv, o1 * inv);
-    if (d == 0 && p.out_lse != nullptr)
-      p.out_lse[row0 + hh] = Z > 0.f ? (M + log2f(Z)) * kLn2 : -INFINITY;
+    // combine the warps through shared memory (the ring's space is free)
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j >= nh) break;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) obuf[(warp * 4 + j) * D + lane * PER + i] = acc[j][i];
+      if (lane == 0) red_l[warp][j] = z[j];
+    }
+    __syncthreads();
+    for (int idx = tid; idx < nh * (D / 2); idx += NW * 32) {
+      const int j = idx / (D / 2), d = 2 * (idx % (D / 2));
+      float Z = 0.f, o0 = 0.f, o1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        Z += red_l[w][j];
+        o0 += obuf[(w * 4 + j) * D + d];
+        o1 += obuf[(w * 4 + j) * D + d + 1];
+      }
+      const float inv = Z > 0.f ? vscale / Z : 0.f;
+      const int hh = h0 + j;
+      *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + (row0 + hh) * D + d) =
+          pack2<QBF16>(o0 * inv, o1 * inv);
+      if (d == 0 && p.out_lse != nullptr)
+        p.out_lse[row0 + hh] = Z > 0.f ? (mbuf[hh] + log2f(Z)) * kLn2 : -INFINITY;
+    }
   }
 }
 
@@ -310,7 +357,7 @@ __global__ void __launch_bounds__(NW * 32)
 #define PKV_DECODE_NST_E4M3 3
 #endif
 #ifndef PKV_DECODE_NST_16
-#define PKV_DECODE_NST_16 3
+#define PKV_DECODE_NST_16 2
 #endif
 
 size_t decode_smem_bytes(int head_dim, pkv_dtype kv_dtype, int G) {
