@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--batch", type=int, default=0,
                     help="override the workload's batch size (profiling on a smaller case)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="skip the CUDA-graph replay timing of the same step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work budget of the oracle baseline sample")
@@ -366,6 +368,10 @@ def run_ours(args):
         attn_mean, achieved = None, None
     traffic = profile_traffic(args.config)
 
+    graph = None
+    if not args.no_graph:
+        graph = measure_graph(step, stream, args, world, kv_bytes, flush, launches_per_step)
+
     e2e = None
     if not args.no_e2e:
         e2e = measure_e2e(step, stream, args, world, kv_bytes, flush)
@@ -415,6 +421,7 @@ def run_ours(args):
             },
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "cuda_graph": graph,
             "clocks": clocks,
             "gpu_launches": launches_per_step * K,
         }
@@ -422,6 +429,42 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def measure_graph(step, stream, args, world, kv_bytes, flush, launches):
+    """The same step captured once into a CUDA graph (cache write, counter
+    reset, decode and, for the mixed step, the prefill on its second stream)
+    and replayed; the L2 flush runs outside the graph, untimed."""
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step.run()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step.run()
+    torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(cur)
+        g.replay()
+        ev[i][1].record(cur)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = allreduce(float(np.mean([a.elapsed_time(b) for a, b in ev])), "max", world)
+    total = allreduce(float(kv_bytes), "sum", world)
+    return {"value": round(total / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+            "ms_per_step": round(ms, 5), "kernels_per_replay": launches}
 
 
 def measure_e2e(step, stream, args, world, kv_bytes, flush):

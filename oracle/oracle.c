@@ -20,6 +20,11 @@
  *    "Decode context parallelism ... merges partial attention by
  *    log-sum-exp"), used to pin that the merge reproduces the unsplit result.
  *  - the causal chunked prefill (Litellama, Features, "Chunked Prefill").
+ *  - the rotary position embedding of the new tokens' queries and keys fused
+ *    with their cache write (rvLLM, Kernel Compiler Stack, "RoPE + KV cache
+ *    write -- fused, no intermediate alloc"; the rotation itself is the
+ *    RoFormer rotary embedding: each pair of dims turned by the angle its
+ *    cos/sin table row gives for the token's position).
  *  - the cache write with the FP8 E4M3 encode (Litellama, Features, "FP8 KV
  *    Cache"; rvLLM, Kernel Compiler Stack, "RoPE + KV cache write"). The
  *    E4M3 format follows the OCP 8-bit floating point specification (OFP8):
@@ -91,6 +96,43 @@ uint8_t pkvo_e4m3_encode(float y) {
   return sign | (uint8_t)(((x + 7) << 3) | ((int)k - 8));
 }
 
+/* Round a double to a 16-bit binary format with p significand bits (hidden
+ * bit included) and `ebits` exponent bits: bias and largest exponent
+ * emax = 2^(ebits-1) - 1, smallest normal exponent emin = 1 - emax. The
+ * result is the nearest value, ties to the even significand; magnitudes past
+ * the largest finite value round to infinity as IEEE-754 round-to-nearest
+ * prescribes; subnormals keep the quantum 2^(emin - p + 1) of the smallest
+ * binade. Returns the bit pattern (sign in bit 15). */
+static uint16_t round_to_binary16(double v, int p, int ebits) {
+  const int fbits = p - 1, emax = (1 << (ebits - 1)) - 1, emin = 1 - emax;
+  const uint16_t sign = signbit(v) ? 0x8000u : 0u;
+  const uint16_t inf = (uint16_t)(((1u << ebits) - 1u) << fbits);
+  if (isnan(v)) return (uint16_t)(inf | (1u << (fbits - 1)));
+  double a = fabs(v);
+  if (isinf(a)) return sign | inf;
+  if (a < ldexp(1.0, emin)) {                          /* subnormal binade */
+    double k = nearbyint(ldexp(a, fbits - emin));      /* grid step 2^(emin-fbits) */
+    return sign | (uint16_t)k;                         /* k = 2^fbits: smallest normal */
+  }
+  int ex;
+  frexp(a, &ex);
+  int x = ex - 1;                                      /* 2^x <= a < 2^(x+1) */
+  double k = nearbyint(ldexp(a, fbits - x));           /* k in [2^fbits, 2^p] */
+  if (k >= ldexp(1.0, p)) { k = ldexp(1.0, fbits); x += 1; }
+  if (x > emax) return sign | inf;
+  return sign | (uint16_t)(((unsigned)(x + emax) << fbits) | ((unsigned)k - (1u << fbits)));
+}
+
+/* IEEE binary16: 11 significand bits, 5 exponent bits. */
+uint16_t pkvo_f16_encode(double v) { return round_to_binary16(v, 11, 5); }
+
+/* bfloat16: 8 significand bits, the 8 exponent bits of binary32. */
+uint16_t pkvo_bf16_encode(double v) { return round_to_binary16(v, 8, 8); }
+
+static uint16_t encode16(double v, int dtype) {
+  return dtype == O_F16 ? pkvo_f16_encode(v) : pkvo_bf16_encode(v);
+}
+
 static double elem(const void* base, int dtype, int64_t i) {
   switch (dtype) {
     case O_F16: return pkvo_f16_value(((const uint16_t*)base)[i]);
@@ -153,6 +195,74 @@ int pkvo_reshape_and_cache(const void* key, const void* value, int src_dtype,
     }
   }
   return bad ? -1 : 0;
+}
+
+/* ---- rotary position embedding ---------------------------------------- */
+
+/* Rotates rows x [T, H, D] (16-bit dtype) by their tokens' positions into
+ * out (same shape and dtype). Row cos_sin[pos] holds rot/2 cosines, then
+ * rot/2 sines. Pair i (i < rot/2) is dims (i, i + rot/2) when neox is set
+ * (the rotate-half convention) and dims (2i, 2i+1) otherwise (interleaved);
+ * for pair (x1, x2) with c, s of row pos:
+ *   y1 = x1 c - x2 s,   y2 = x2 c + x1 s,
+ * both products exact in double (a 16-bit value times a binary32 value needs
+ * at most 35 significand bits), one rounding for the sum, then one rounding
+ * to the row dtype. Dims from rot on are copied. A token whose position is
+ * outside [0, max_pos) is copied unrotated and sets bit 2 of the result. */
+int pkvo_rope(const void* x, int dtype, int T, int H, int D, const int64_t* pos,
+              const float* cos_sin, int64_t max_pos, int rot, int neox, void* out) {
+  int bad = 0;
+  const uint16_t* xs = (const uint16_t*)x;
+  uint16_t* ys = (uint16_t*)out;
+  const int half = rot / 2;
+  for (int t = 0; t < T; ++t) {
+    const int64_t p = pos[t];
+    const int ok = p >= 0 && p < max_pos;
+    if (!ok) bad = 2;
+    for (int h = 0; h < H; ++h) {
+      const int64_t row = ((int64_t)t * H + h) * D;
+      for (int d = 0; d < D; ++d) ys[row + d] = xs[row + d];
+      if (!ok) continue;
+      const float* cs = cos_sin + p * rot;
+      for (int i = 0; i < half; ++i) {
+        const int d1 = neox ? i : 2 * i;
+        const int d2 = neox ? i + half : 2 * i + 1;
+        const double x1 = elem(x, dtype, row + d1), x2 = elem(x, dtype, row + d2);
+        const double c = (double)cs[i], sn = (double)cs[half + i];
+        const double y1 = x1 * c - x2 * sn;
+        const double y2 = x2 * c + x1 * sn;
+        ys[row + d1] = encode16(y1, dtype);
+        ys[row + d2] = encode16(y2, dtype);
+      }
+    }
+  }
+  return bad;
+}
+
+/* The fused step: rotate the queries (into q_out) and the keys, then write
+ * the rotated keys, rounded to the source dtype, and the values into their
+ * slots exactly as pkvo_reshape_and_cache does. Tokens with a position
+ * outside [0, max_pos) keep their query unrotated and write nothing.
+ * Returns a bit set: 1 = some slot outside the pool, 2 = some position
+ * outside the table. */
+int pkvo_rope_reshape_and_cache(const void* q, const void* key, const void* value, int src_dtype,
+                                void* k_cache, void* v_cache, int kv_dtype,
+                                const int64_t* slots, const int64_t* pos, const float* cos_sin,
+                                int64_t max_pos, int rot, int neox, int T, int Hq, int Hkv,
+                                int D, int BS, int num_blocks, const float* k_scales,
+                                const float* v_scales, void* q_out) {
+  int flags = pkvo_rope(q, src_dtype, T, Hq, D, pos, cos_sin, max_pos, rot, neox, q_out);
+  uint16_t* krot = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)T * Hkv * D + 1);
+  int64_t* sl = (int64_t*)malloc(sizeof(int64_t) * (size_t)T + 1);
+  if (krot == NULL || sl == NULL) { free(krot); free(sl); return -1; }
+  flags |= pkvo_rope(key, src_dtype, T, Hkv, D, pos, cos_sin, max_pos, rot, neox, krot);
+  for (int t = 0; t < T; ++t) sl[t] = (pos[t] >= 0 && pos[t] < max_pos) ? slots[t] : -1;
+  if (pkvo_reshape_and_cache(krot, value, src_dtype, k_cache, v_cache, kv_dtype, sl, T, Hkv, D,
+                             BS, num_blocks, k_scales, v_scales) != 0)
+    flags |= 1;
+  free(krot);
+  free(sl);
+  return flags;
 }
 
 /* ---- attention over one sequence and head ----------------------------- */

@@ -51,6 +51,15 @@ def lib():
         L.pkvo_e4m3_value.argtypes = [ctypes.c_uint8]
         L.pkvo_e4m3_encode.restype = ctypes.c_uint8
         L.pkvo_e4m3_encode.argtypes = [ctypes.c_float]
+        L.pkvo_f16_encode.restype = ctypes.c_uint16
+        L.pkvo_f16_encode.argtypes = [D]
+        L.pkvo_bf16_encode.restype = ctypes.c_uint16
+        L.pkvo_bf16_encode.argtypes = [D]
+        L.pkvo_rope.restype = I
+        L.pkvo_rope.argtypes = [P, I, I, I, I, P, P, I64, I, I, P]
+        L.pkvo_rope_reshape_and_cache.restype = I
+        L.pkvo_rope_reshape_and_cache.argtypes = [P, P, P, I, P, P, I, P, P, P, I64, I, I, I, I,
+                                                  I, I, I, I, P, P, P]
         L.pkvo_set_threads.argtypes = [I]
         L.pkvo_get_threads.restype = I
         L.pkvo_reshape_and_cache.restype = I
@@ -101,6 +110,52 @@ def e4m3_value(code: int) -> float:
 
 def e4m3_encode(y: float) -> int:
     return int(lib().pkvo_e4m3_encode(float(np.float32(y))))
+
+
+def f16_encode(v: float) -> int:
+    """Bits of the binary16 nearest to v (ties to even)."""
+    return int(lib().pkvo_f16_encode(float(v)))
+
+
+def bf16_encode(v: float) -> int:
+    """Bits of the bfloat16 nearest to v (ties to even)."""
+    return int(lib().pkvo_bf16_encode(float(v)))
+
+
+def rope(x, positions, cos_sin, rot_dim: int, neox: bool = True):
+    """Rotary embedding of rows x [T, H, D] (fp16/bf16, CPU) by their tokens'
+    positions with the fp32 table cos_sin [max_position, rot_dim] (cosines,
+    then sines). Returns (rotated rows, same dtype; flags: 2 if a position was
+    outside the table)."""
+    T, H, D = x.shape
+    pos = _np(positions, np.int64)
+    cs = _np(cos_sin, np.float32)
+    out = torch.empty_like(x)
+    rc = lib().pkvo_rope(_ptr(x), _DT[x.dtype], T, H, D, _ptr(pos), _ptr(cs), int(cs.shape[0]),
+                         int(rot_dim), int(bool(neox)), _ptr(out))
+    return out, int(rc)
+
+
+def rope_reshape_and_cache(q, key, value, k_cache, v_cache, slots, positions, cos_sin,
+                           rot_dim: int, neox: bool = True, k_scales=None, v_scales=None):
+    """The fused step: rotated queries (returned) and the rotated keys plus
+    the values written into the caches in place. Returns (q_out, flags) with
+    flags bit 1 = a slot outside the pool, bit 2 = a position outside the
+    table."""
+    T, Hq, D = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    pos = _np(positions, np.int64)
+    sl = _np(slots, np.int64)
+    cs = _np(cos_sin, np.float32)
+    ks, vs = _np(k_scales, np.float32), _np(v_scales, np.float32)
+    q_out = torch.empty_like(q)
+    rc = lib().pkvo_rope_reshape_and_cache(
+        _ptr(q), _ptr(key), _ptr(value), _DT[q.dtype], _ptr(k_cache), _ptr(v_cache),
+        _DT[k_cache.dtype], _ptr(sl), _ptr(pos), _ptr(cs), int(cs.shape[0]), int(rot_dim),
+        int(bool(neox)), T, Hq, hkv, D, bs, nb, _ptr(ks), _ptr(vs), _ptr(q_out))
+    if rc < 0:
+        raise MemoryError("oracle rope_reshape_and_cache: out of host memory")
+    return q_out, int(rc)
 
 
 def reshape_and_cache(key, value, k_cache, v_cache, slots, k_scales=None, v_scales=None) -> int:

@@ -21,6 +21,10 @@ Recipe (all draws seeded):
     block beyond its context hold a large finite sentinel (60.0, or code
     0x7E = 448 for FP8), so a read past the context shows as a large error.
 
+Rotary tables (`rope_cos_sin`) are model inputs, like weights: row p holds
+cos and sin of p * base^(-2i/rot) for i < rot/2, the angles taken in double
+and rounded to fp32 once.
+
 A decode step caches, for every sequence, positions 0 .. ctx-2 ("fill" rows,
 already in the cache before the step) and writes position ctx-1 ("new" rows,
 written by the step's reshape_and_cache). The prefill chunk's sequence has P
@@ -80,6 +84,7 @@ class Case:
     new_k: torch.Tensor             # [Tn, Hkv, D]
     new_v: torch.Tensor
     new_slots: np.ndarray           # int64 [Tn]
+    new_positions: np.ndarray       # int64 [Tn] the new rows' positions in their sequences
     tail_slots: np.ndarray          # int64: slots past a context in its last block
     k_scales: Optional[np.ndarray]  # fp32 [Hkv] (FP8 only)
     v_scales: Optional[np.ndarray]
@@ -240,20 +245,23 @@ def make_case(name: str | dict = "tiny", seed: int = 0, device: str = "cpu",
     def slots_of(row, positions):
         return row[positions // BS].astype(np.int64) * BS + positions % BS
 
-    fill_slots, new_slots, tail = [], [], []
+    fill_slots, new_slots, tail, new_pos = [], [], [], []
     for b in range(B):
         c = int(ctx[b])
         start = sp[1] if (sp is not None and 0 < b < sp[0]) else 0
         fill_slots.append(slots_of(tables[b], np.arange(start, c - 1, dtype=np.int64)))
         if c > 0:
             new_slots.append(slots_of(tables[b], np.array([c - 1], np.int64)))
+            new_pos.append(np.array([c - 1], np.int64))
         tail.append(slots_of(tables[b], np.arange(c, int(nblk[b]) * BS, dtype=np.int64)))
     if pf is not None:
         fill_slots.append(slots_of(pf_table[0], np.arange(0, P, dtype=np.int64)))
         new_slots.append(slots_of(pf_table[0], np.arange(P, P + L, dtype=np.int64)))
+        new_pos.append(np.arange(P, P + L, dtype=np.int64))
         tail.append(slots_of(pf_table[0], np.arange(P + L, pf_blocks * BS, dtype=np.int64)))
     cat = lambda xs: np.concatenate(xs) if xs else np.zeros(0, np.int64)
     fill_slots, new_slots, tail_slots = cat(fill_slots), cat(new_slots), cat(tail)
+    new_positions = cat(new_pos)
 
     # --- values --------------------------------------------------------------
     q = torch.randn((B, Hq, D), generator=_gen(seed, 1, device), device=device,
@@ -283,8 +291,20 @@ def make_case(name: str | dict = "tiny", seed: int = 0, device: str = "cpu",
         num_blocks=num_blocks, max_blocks_per_seq=max_blocks,
         poison_block=poison, q=q, fill_k=fill_k, fill_v=fill_v,
         fill_slots=fill_slots, new_k=new_k, new_v=new_v, new_slots=new_slots,
+        new_positions=new_positions,
         tail_slots=tail_slots, k_scales=k_scales, v_scales=v_scales,
         prefill=prefill, shared_blocks=shared, device=device)
+
+
+def rope_cos_sin(max_position: int, rot_dim: int, base: float = 10000.0) -> np.ndarray:
+    """A model's rotary table, fp32 [max_position, rot_dim]: row p is
+    cos(p w_i) for i < rot_dim/2, then sin(p w_i), with w_i = base^(-2i/rot_dim)
+    (angles in double, one rounding to fp32)."""
+    assert rot_dim % 2 == 0
+    i = np.arange(rot_dim // 2, dtype=np.float64)
+    w = base ** (-2.0 * i / rot_dim)
+    ang = np.arange(max_position, dtype=np.float64)[:, None] * w[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
 
 
 def empty_cache(case: Case, device: Optional[str] = None):
