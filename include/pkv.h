@@ -15,8 +15,9 @@
  *  - partial attention "merged by log-sum-exp" (rapid_llm README, feature
  *    table, row "Decode context parallelism"), done here over KV partitions
  *    of one GPU.
- *  - "RoPE + KV cache write" (rvLLM, Kernel Compiler Stack, decode step at
- *    c=128): the cache-write half is reshape_and_cache below.
+ *  - "RoPE + KV cache write -- fused, no intermediate alloc" (rvLLM, Kernel
+ *    Compiler Stack, decode step at c=128): rope_reshape_and_cache below; its
+ *    cache-write half alone is reshape_and_cache.
  *  - "FP8 KV Cache" (Litellama, Features; rvLLM, Optional Features):
  *    E4M3 codes with one fp32 scale per KV head for K and one for V.
  *  - "Chunked Prefill ... 512-token chunks" (Litellama, Features): causal
@@ -80,6 +81,7 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
 #define PKV_DEVERR_SEQ_LEN    0x4u  /* seq_len < 0 or above the stated maximum */
 #define PKV_DEVERR_TIMEOUT    0x8u  /* a bounded wait on an async copy gave up */
 #define PKV_DEVERR_QLEN       0x10u /* prefill: chunk longer than its context */
+#define PKV_DEVERR_POSITION   0x20u /* rotary: position outside [0, max_position) */
 
 /*
  * paged_attn_decode_workspace_size
@@ -215,6 +217,43 @@ pkv_status reshape_and_cache(const void* key, const void* value,
                              int block_size, int num_blocks,
                              const float* k_scales, const float* v_scales,
                              void* stream);
+
+/*
+ * rope_reshape_and_cache — the rotary position embedding of the new tokens'
+ * queries and keys, fused with the cache write of their keys and values
+ * (rvLLM, Kernel Compiler Stack, "RoPE + KV cache write -- fused, no
+ * intermediate alloc"). The rotation is the rotary embedding of RoFormer:
+ * each pair of dims of a head is turned by the angle of the token's position.
+ *   query:  [num_tokens, Hq, D] src_dtype, rotated IN PLACE.
+ *   key, value: [num_tokens, Hkv, D] src_dtype, read only; the rotated key
+ *           is not stored anywhere but in the cache.
+ *   positions: int64 [num_tokens], the token's position in its sequence.
+ *   cos_sin_cache: fp32 [max_position, rot_dim]; row p holds rot_dim/2
+ *           cosines, then rot_dim/2 sines (the model's rotary table).
+ *   rot_dim: rotated dims per head, a multiple of 16 in [16, D]; dims from
+ *           rot_dim on pass through unchanged.
+ *   neox_style: nonzero = pair i is dims (i, i + rot_dim/2) (rotate-half);
+ *           zero = pair i is dims (2i, 2i+1) (interleaved).
+ *   For pair (x1, x2) and (c, s) = row positions[t], entries i, rot_dim/2+i:
+ *     y1 = x1 c - x2 s,  y2 = x2 c + x1 s
+ *   with both products exact in double, one rounding of the sum to double
+ *   and one round-to-nearest-even to src_dtype. The key's rotated row, in
+ *   src_dtype, and the value row are then written to slot_mapping[t] exactly
+ *   as reshape_and_cache writes them (bit copy, or the E4M3 encode with
+ *   k_scales / v_scales). Slot < 0: the query is still rotated, nothing is
+ *   written. A position outside [0, max_position) sets PKV_DEVERR_POSITION:
+ *   that token's query is left as it was and nothing is written; a slot
+ *   >= num_blocks * BS sets PKV_DEVERR_SLOT and writes nothing.
+ */
+pkv_status rope_reshape_and_cache(void* query, const void* key, const void* value,
+                                  pkv_dtype src_dtype, void* k_cache, void* v_cache,
+                                  pkv_dtype kv_dtype, const int64_t* slot_mapping,
+                                  const int64_t* positions, const float* cos_sin_cache,
+                                  int max_position, int rot_dim, int neox_style,
+                                  int num_tokens, int num_q_heads, int num_kv_heads,
+                                  int head_dim, int block_size, int num_blocks,
+                                  const float* k_scales, const float* v_scales,
+                                  void* stream);
 
 /*
  * pkv_get_device_error — synchronises `stream`, then reads and clears the

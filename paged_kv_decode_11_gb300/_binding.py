@@ -19,12 +19,13 @@ LIB_PATH = os.path.join(HERE, "libpkv.so")
 PKV_F16, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
           3: "workspace missing or too small", 4: "CUDA error", 5: "device-side check failed"}
-DEVERR_BITS = {0x1: "block id", 0x2: "slot", 0x4: "seq_len", 0x8: "timeout", 0x10: "chunk length"}
+DEVERR_BITS = {0x1: "block id", 0x2: "slot", 0x4: "seq_len", 0x8: "timeout", 0x10: "chunk length",
+               0x20: "rotary position"}
 
 # Every symbol include/pkv.h declares.
 EXPORTS = ("paged_attn_decode_workspace_size", "paged_attn_decode", "paged_attn_decode_noalloc",
-           "paged_attn_prefill_chunk", "reshape_and_cache", "pkv_get_device_error",
-           "pkv_status_string")
+           "paged_attn_prefill_chunk", "reshape_and_cache", "rope_reshape_and_cache",
+           "pkv_get_device_error", "pkv_status_string")
 
 _lib = None
 
@@ -61,6 +62,9 @@ def load(path: str = LIB_PATH):
                                            F, P, P, P, P]
     L.reshape_and_cache.restype = I
     L.reshape_and_cache.argtypes = [P, P, I, P, P, I, P, I, I, I, I, I, P, P, P]
+    L.rope_reshape_and_cache.restype = I
+    L.rope_reshape_and_cache.argtypes = [P, P, P, I, P, P, I, P, P, P, I, I, I, I, I, I, I, I,
+                                         I, P, P, P]
     L.pkv_get_device_error.restype = I
     L.pkv_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
     L.pkv_status_string.restype = ctypes.c_char_p
@@ -194,6 +198,32 @@ def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Ten
         _dev_ptr(slot_mapping, "slot_mapping"), T, hkv, D, bs, nb,
         _dev_ptr(k_scales, "k_scales"), _dev_ptr(v_scales, "v_scales"), _stream(stream))
     _check("reshape_and_cache", st)
+
+
+def rope_reshape_and_cache(query: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
+                           k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           slot_mapping: torch.Tensor, positions: torch.Tensor,
+                           cos_sin_cache: torch.Tensor, rot_dim: Optional[int] = None,
+                           neox_style: bool = True, k_scales: Optional[torch.Tensor] = None,
+                           v_scales: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Rotate query [T, Hq, D] in place and key [T, Hkv, D] by their
+    positions with the fp32 table cos_sin_cache [max_position, rot_dim], and
+    write the rotated keys and the values into their cache slots."""
+    T, Hq, D = query.shape
+    nb, hkv, bs, _ = k_cache.shape
+    assert key.shape == (T, hkv, D) and value.shape == key.shape
+    assert slot_mapping.dtype == torch.int64 and positions.dtype == torch.int64
+    assert cos_sin_cache.dtype == torch.float32 and cos_sin_cache.dim() == 2
+    rot = cos_sin_cache.shape[1] if rot_dim is None else int(rot_dim)
+    assert cos_sin_cache.shape[1] == rot
+    st = load().rope_reshape_and_cache(
+        _dev_ptr(query, "query"), _dev_ptr(key, "key"), _dev_ptr(value, "value"),
+        dtype_code(query), _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"),
+        dtype_code(k_cache), _dev_ptr(slot_mapping, "slot_mapping"),
+        _dev_ptr(positions, "positions"), _dev_ptr(cos_sin_cache, "cos_sin_cache"),
+        cos_sin_cache.shape[0], rot, int(bool(neox_style)), T, Hq, hkv, D, bs, nb,
+        _dev_ptr(k_scales, "k_scales"), _dev_ptr(v_scales, "v_scales"), _stream(stream))
+    _check("rope_reshape_and_cache", st)
 
 
 def pkv_get_device_error(stream=None) -> int:

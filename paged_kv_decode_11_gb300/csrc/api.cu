@@ -312,6 +312,54 @@ pkv_status reshape_and_cache(const void* key, const void* value, pkv_dtype src_d
   return launch_cache_write(p, src_dtype, kv_dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
+pkv_status rope_reshape_and_cache(void* query, const void* key, const void* value,
+                                  pkv_dtype src_dtype, void* k_cache, void* v_cache,
+                                  pkv_dtype kv_dtype, const int64_t* slot_mapping,
+                                  const int64_t* positions, const float* cos_sin_cache,
+                                  int max_position, int rot_dim, int neox_style, int num_tokens,
+                                  int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                  int num_blocks, const float* k_scales, const float* v_scales,
+                                  void* stream) {
+  if (num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
+      max_position <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if (!valid_dtypes(src_dtype, kv_dtype)) return PKV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (block_size != 16) return PKV_ERR_UNSUPPORTED;
+  if (rot_dim < 16 || rot_dim > head_dim || rot_dim % 16 != 0) return PKV_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!query || !key || !value || !k_cache || !v_cache || !slot_mapping || !positions ||
+      !cos_sin_cache)
+    return PKV_ERR_INVALID_ARG;
+  if (kv_dtype == PKV_FP8_E4M3 && (!k_scales || !v_scales)) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(query) || !aligned16(key) || !aligned16(value) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(cos_sin_cache))
+    return PKV_ERR_INVALID_ARG;
+  unsigned int* err = err_word();
+  if (err == nullptr) return PKV_ERR_CUDA;
+  RopeCacheParams p{};
+  p.query = query;
+  p.key = key;
+  p.value = value;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.slots = slot_mapping;
+  p.positions = positions;
+  p.cos_sin = cos_sin_cache;
+  p.k_scales = k_scales;
+  p.v_scales = v_scales;
+  p.err = err;
+  p.max_position = max_position;
+  p.rot = rot_dim;
+  p.neox = neox_style != 0;
+  p.num_tokens = num_tokens;
+  p.Hq = num_q_heads;
+  p.Hkv = num_kv_heads;
+  p.D = head_dim;
+  p.num_blocks = num_blocks;
+  return launch_rope_cache(p, src_dtype, kv_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
 pkv_status pkv_get_device_error(void* stream, unsigned int* bits) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
     return PKV_ERR_CUDA;

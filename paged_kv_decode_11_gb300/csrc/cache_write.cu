@@ -14,6 +14,7 @@
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 #include "common.cuh"
+#include "kv_store.cuh"
 #include "launch.h"
 
 namespace pkv {
@@ -34,41 +35,13 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const CacheWriteParams
     if (h == 0 && ch == 0) atomicOr(p.err, PKV_DEVERR_SLOT);
     return;
   }
-  const int64_t dst = (((slot / kBS) * p.Hkv + h) * kBS + (slot % kBS)) * p.D + ch * 8;
+  const int64_t dst = cache_elem(slot, h, p.Hkv, p.D, ch * 8);
   const int64_t src = row * p.D + ch * 8;
   const uint4 kin = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.key) + src);
   const uint4 vin = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.value) + src);
-  if constexpr (!TO_FP8) {
-    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.k_cache) + dst) = kin;
-    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.v_cache) + dst) = vin;
-  } else {
-    const float ks = p.k_scales[h], vs = p.v_scales[h];
-    auto enc = [](const uint4& in, float s) -> uint2 {
-      const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-      uint32_t out[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        float f[4];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const uint32_t word = w[2 * j + e];
-          if constexpr (SRC_BF16) {
-            f[2 * e] = __uint_as_float(word << 16);
-            f[2 * e + 1] = __uint_as_float(word & 0xFFFF0000u);
-          } else {
-            f[2 * e] = __half2float(__ushort_as_half(static_cast<unsigned short>(word & 0xFFFFu)));
-            f[2 * e + 1] = __half2float(__ushort_as_half(static_cast<unsigned short>(word >> 16)));
-          }
-        }
-        const uint32_t lo = f32x2_to_e4m3x2(__fdiv_rn(f[0], s), __fdiv_rn(f[1], s));
-        const uint32_t hi = f32x2_to_e4m3x2(__fdiv_rn(f[2], s), __fdiv_rn(f[3], s));
-        out[j] = lo | (hi << 16);
-      }
-      return make_uint2(out[0], out[1]);
-    };
-    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.k_cache) + dst) = enc(kin, ks);
-    *reinterpret_cast<uint2*>(static_cast<uint8_t*>(p.v_cache) + dst) = enc(vin, vs);
-  }
+  const float ks = TO_FP8 ? p.k_scales[h] : 1.f, vs = TO_FP8 ? p.v_scales[h] : 1.f;
+  store_row8<SRC_BF16, TO_FP8>(p.k_cache, dst, kin, ks);
+  store_row8<SRC_BF16, TO_FP8>(p.v_cache, dst, vin, vs);
 }
 
 pkv_status launch_cache_write(const CacheWriteParams& p, pkv_dtype src_dtype, pkv_dtype kv_dtype,

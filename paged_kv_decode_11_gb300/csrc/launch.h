@@ -54,6 +54,22 @@ struct CacheWriteParams {
   int num_tokens, Hkv, D, num_blocks;
 };
 
+struct RopeCacheParams {
+  void* query;
+  const void* key;
+  const void* value;
+  void* k_cache;
+  void* v_cache;
+  const int64_t* slots;
+  const int64_t* positions;
+  const float* cos_sin;
+  const float* k_scales;
+  const float* v_scales;
+  unsigned int* err;
+  int64_t max_position;
+  int rot, neox, num_tokens, Hq, Hkv, D, num_blocks;
+};
+
 // Each launcher validates nothing (the entry points do) and returns
 // PKV_ERR_CUDA on a launch failure.
 pkv_status launch_decode(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
@@ -66,6 +82,8 @@ pkv_status launch_prefill(const PrefillParams& p, int head_dim, pkv_dtype q_dtyp
                           cudaStream_t stream);
 pkv_status launch_cache_write(const CacheWriteParams& p, pkv_dtype src_dtype,
                               pkv_dtype kv_dtype, cudaStream_t stream);
+pkv_status launch_rope_cache(const RopeCacheParams& p, pkv_dtype src_dtype, pkv_dtype kv_dtype,
+                             cudaStream_t stream);
 
 // Rows of q handled by one prefill CTA for a GQA group size G.
 int prefill_q_tile(int G);

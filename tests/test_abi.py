@@ -133,3 +133,25 @@ def _cache(lib, **kw):
 ])
 def test_cache_write_argument_checks(lib, kw, want):
     assert _cache(lib, **kw) == want
+
+
+def _rope(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, src=BF16, kc=FAKE, vc=FAKE, kv=FP8, slots=FAKE, pos=FAKE,
+             cs=FAKE, maxpos=4096, rot=128, neox=1, T=4, Hq=8, Hkv=2, D=128, BS=16, nb=8,
+             ks=FAKE, vs=FAKE, stream=None)
+    a.update(kw)
+    return lib.rope_reshape_and_cache(a["q"], a["k"], a["v"], a["src"], a["kc"], a["vc"], a["kv"],
+                                      a["slots"], a["pos"], a["cs"], a["maxpos"], a["rot"],
+                                      a["neox"], a["T"], a["Hq"], a["Hkv"], a["D"], a["BS"],
+                                      a["nb"], a["ks"], a["vs"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(rot=0), INVALID), (dict(rot=24), INVALID), (dict(rot=144), INVALID),
+    (dict(D=64, rot=128), INVALID), (dict(maxpos=0), INVALID), (dict(pos=None), INVALID),
+    (dict(cs=None), INVALID), (dict(cs=FAKE + 8), INVALID), (dict(q=None), INVALID),
+    (dict(ks=None), INVALID), (dict(src=FP8), UNSUPPORTED), (dict(BS=32), UNSUPPORTED),
+    (dict(T=0, q=None, k=None), OK), (dict(Hq=0), INVALID),
+])
+def test_rope_cache_argument_checks(lib, kw, want):
+    assert _rope(lib, **kw) == want
