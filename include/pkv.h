@@ -49,8 +49,9 @@
  *                              K/V reshape_and_cache has already written
  *    Logical token j of sequence b lives in physical block
  *    block_tables[b][j / BS] at offset j % BS. Query head h reads KV head
- *    h / G. Within a block each KV head's BS x D page is one contiguous run.
- *  - Supported: D in {64, 128}; BS == 16; G <= 16; q dtype F16 or BF16; KV
+ *    h / G. Within a block each KV head's BS x D run is contiguous; the
+ *    kernels read it as BS / 16 consecutive pages of 16 tokens.
+ *  - Supported: D in {64, 128}; BS in {16, 32, 64}; G <= 16; q dtype F16 or BF16; KV
  *    dtype equal to the q dtype, or FP8_E4M3 with per-KV-head fp32 scales
  *    (dequantised value = code * scale).
  */

@@ -76,8 +76,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // Tensor map {D, 16, num_blocks * Hkv} over a cache [num_blocks, Hkv, 16, D]:
 // one box is 16 page rows by min(row bytes, 128) bytes, swizzled so that
 // the fragment loads of the kernels are bank-conflict free.
+// log2 of the 16-token pages in a block of `block_size` tokens (16, 32 or 64),
+// or -1 for a size the kernels do not take.
+int page_shift(int block_size) {
+  return block_size == 16 ? 0 : block_size == 32 ? 1 : block_size == 64 ? 2 : -1;
+}
+
+// Page rows and per-sequence token counts stay within int32.
+bool page_rows_fit(int num_blocks, int Hkv, int shift, int max_blocks_per_seq, int block_size) {
+  return (((int64_t)num_blocks * Hkv) << shift) < ((int64_t)1 << 31) &&
+         (int64_t)max_blocks_per_seq * block_size < ((int64_t)1 << 30);
+}
+
+// A cache as the tensor maps see it: {D, 16 rows, num_blocks * Hkv * pages
+// per block} (innermost first); page row z = (block * Hkv + head) * ppb + sub.
 bool make_kv_tmap(CUtensorMap* m, const void* base, pkv_dtype dt, int D, int Hkv,
-                  int num_blocks) {
+                  int num_blocks, int ppb_shift) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const int elt = dt == PKV_FP8_E4M3 ? 1 : 2;
@@ -86,7 +100,8 @@ bool make_kv_tmap(CUtensorMap* m, const void* base, pkv_dtype dt, int D, int Hkv
   CUtensorMapDataType t = dt == PKV_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                           : dt == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                            : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  cuuint64_t dims[3] = {(cuuint64_t)D, 16, (cuuint64_t)num_blocks * (cuuint64_t)Hkv};
+  cuuint64_t dims[3] = {(cuuint64_t)D, 16,
+                        ((cuuint64_t)num_blocks * (cuuint64_t)Hkv) << ppb_shift};
   cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)row_bytes * 16};
   cuuint32_t box[3] = {(cuuint32_t)(box_row / elt), 16, 1};
   cuuint32_t es[3] = {1, 1, 1};
@@ -173,7 +188,10 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const 
     return PKV_ERR_INVALID_ARG;
   if (!valid_dtypes(q_dtype, kv_dtype)) return PKV_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (block_size != 16) return PKV_ERR_UNSUPPORTED;
+  const int shift = page_shift(block_size);
+  if (shift < 0) return PKV_ERR_UNSUPPORTED;
+  if (!page_rows_fit(num_blocks, num_kv_heads, shift, max_blocks_per_seq, block_size))
+    return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / num_kv_heads;
   if (G > 16) return PKV_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
@@ -191,8 +209,8 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const 
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return PKV_ERR_WORKSPACE;
   CUtensorMap tmK, tmV;
-  if (!make_kv_tmap(&tmK, k_cache, kv_dtype, head_dim, num_kv_heads, num_blocks) ||
-      !make_kv_tmap(&tmV, v_cache, kv_dtype, head_dim, num_kv_heads, num_blocks))
+  if (!make_kv_tmap(&tmK, k_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift) ||
+      !make_kv_tmap(&tmV, v_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift))
     return PKV_ERR_CUDA;
   unsigned int* err = err_word();
   if (err == nullptr) return PKV_ERR_CUDA;
@@ -220,6 +238,7 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const 
   p.max_blocks = max_blocks_per_seq;
   p.num_blocks = num_blocks;
   p.max_seq_len = max_seq_len;
+  p.ppb_shift = shift;
   p.part = pl.part;
   p.max_parts = pl.max_parts;
   p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
@@ -241,7 +260,10 @@ pkv_status paged_attn_prefill_chunk(void* out, const void* q, pkv_dtype q_dtype,
   if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   if (!valid_dtypes(q_dtype, kv_dtype)) return PKV_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (block_size != 16) return PKV_ERR_UNSUPPORTED;
+  const int shift = page_shift(block_size);
+  if (shift < 0) return PKV_ERR_UNSUPPORTED;
+  if (!page_rows_fit(num_blocks, num_kv_heads, shift, max_blocks_per_seq, block_size))
+    return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / num_kv_heads;
   if (G > 16) return PKV_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
@@ -252,8 +274,8 @@ pkv_status paged_attn_prefill_chunk(void* out, const void* q, pkv_dtype q_dtype,
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_ERR_INVALID_ARG;
   CUtensorMap tmK, tmV;
-  if (!make_kv_tmap(&tmK, k_cache, kv_dtype, head_dim, num_kv_heads, num_blocks) ||
-      !make_kv_tmap(&tmV, v_cache, kv_dtype, head_dim, num_kv_heads, num_blocks))
+  if (!make_kv_tmap(&tmK, k_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift) ||
+      !make_kv_tmap(&tmV, v_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift))
     return PKV_ERR_CUDA;
   unsigned int* err = err_word();
   if (err == nullptr) return PKV_ERR_CUDA;
@@ -275,6 +297,7 @@ pkv_status paged_attn_prefill_chunk(void* out, const void* q, pkv_dtype q_dtype,
   p.num_blocks = num_blocks;
   p.max_q_len = max_q_len;
   p.q_tile = prefill_q_tile(G);
+  p.ppb_shift = shift;
   p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   return launch_prefill(p, head_dim, q_dtype, kv_dtype, tmK, tmV,
                         reinterpret_cast<cudaStream_t>(stream));
@@ -288,7 +311,8 @@ pkv_status reshape_and_cache(const void* key, const void* value, pkv_dtype src_d
   if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
   if (!valid_dtypes(src_dtype, kv_dtype)) return PKV_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (block_size != 16) return PKV_ERR_UNSUPPORTED;
+  const int shift = page_shift(block_size);
+  if (shift < 0) return PKV_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PKV_OK;
   if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
   if (kv_dtype == PKV_FP8_E4M3 && (!k_scales || !v_scales)) return PKV_ERR_INVALID_ARG;
@@ -309,6 +333,7 @@ pkv_status reshape_and_cache(const void* key, const void* value, pkv_dtype src_d
   p.Hkv = num_kv_heads;
   p.D = head_dim;
   p.num_blocks = num_blocks;
+  p.bs_log2 = 4 + shift;
   return launch_cache_write(p, src_dtype, kv_dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -325,7 +350,8 @@ pkv_status rope_reshape_and_cache(void* query, const void* key, const void* valu
     return PKV_ERR_INVALID_ARG;
   if (!valid_dtypes(src_dtype, kv_dtype)) return PKV_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  if (block_size != 16) return PKV_ERR_UNSUPPORTED;
+  const int shift = page_shift(block_size);
+  if (shift < 0) return PKV_ERR_UNSUPPORTED;
   if (rot_dim < 16 || rot_dim > head_dim || rot_dim % 16 != 0) return PKV_ERR_INVALID_ARG;
   if (num_tokens == 0) return PKV_OK;
   if (!query || !key || !value || !k_cache || !v_cache || !slot_mapping || !positions ||
@@ -357,6 +383,7 @@ pkv_status rope_reshape_and_cache(void* query, const void* key, const void* valu
   p.Hkv = num_kv_heads;
   p.D = head_dim;
   p.num_blocks = num_blocks;
+  p.bs_log2 = 4 + shift;
   return launch_rope_cache(p, src_dtype, kv_dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 

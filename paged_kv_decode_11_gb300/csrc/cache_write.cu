@@ -31,11 +31,11 @@ __global__ void __launch_bounds__(256) cache_write_kernel(const CacheWriteParams
   const int64_t t = row / p.Hkv;
   const int64_t slot = p.slots[t];
   if (slot < 0) return;
-  if (slot >= (int64_t)p.num_blocks * kBS) {
+  if (slot >= ((int64_t)p.num_blocks << p.bs_log2)) {
     if (h == 0 && ch == 0) atomicOr(p.err, PKV_DEVERR_SLOT);
     return;
   }
-  const int64_t dst = cache_elem(slot, h, p.Hkv, p.D, ch * 8);
+  const int64_t dst = cache_elem(slot, h, p.Hkv, p.D, ch * 8, p.bs_log2);
   const int64_t src = row * p.D + ch * 8;
   const uint4 kin = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.key) + src);
   const uint4 vin = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.value) + src);

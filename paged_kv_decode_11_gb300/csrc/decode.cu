@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(NW * 32)
   const int G = p.G;
 
   int ctx = p.seq_lens[b];
-  const int cap = min(p.max_seq_len, p.max_blocks * kBS);
+  const int cap = min(p.max_seq_len, (p.max_blocks * kBS) << p.ppb_shift);
   if (ctx < 0 || ctx > cap) {
     if (tid == 0 && part_idx == 0 && h == 0) atomicOr(p.err, PKV_DEVERR_SEQ_LEN);
     ctx = ctx < 0 ? 0 : cap;
@@ -76,13 +76,17 @@ __global__ void __launch_bounds__(NW * 32)
   const uint32_t base = (raw_base + 1023u) & ~1023u;
   uint8_t* basep = smem_raw + (base - raw_base);
 
+  // page rows of the tensor maps: a block of 16 << ppb_shift tokens holds that
+  // many consecutive 16-token pages per KV head
+  const int sub_mask = (1 << p.ppb_shift) - 1;
   for (int i = tid; i < npages; i += NW * 32) {
-    int id = p.block_tables[(int64_t)b * p.max_blocks + page0 + i];
+    const int pg = page0 + i;
+    int id = p.block_tables[(int64_t)b * p.max_blocks + (pg >> p.ppb_shift)];
     if (id < 0 || id >= p.num_blocks) {
       atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
       id = 0;
     }
-    s_ids[i] = id;
+    s_ids[i] = ((id * p.Hkv + h) << p.ppb_shift) + (pg & sub_mask);
   }
   if (tid == 0) {
     prefetch_tensormap(&tmK);
@@ -102,7 +106,7 @@ __global__ void __launch_bounds__(NW * 32)
   auto issue = [&](int k) {
     const int st = k % NST;
     uint64_t* bar = &bars[warp][st];
-    const int z = s_ids[warp + NW * k] * p.Hkv + h;
+    const int z = s_ids[warp + NW * k];
     uint8_t* dst = wbasep + st * STAGE;
     mbar_arrive_expect_tx(bar, STAGE);
 #pragma unroll

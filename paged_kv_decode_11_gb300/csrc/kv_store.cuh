@@ -58,9 +58,11 @@ __device__ __forceinline__ void store_row8(void* cache, int64_t idx, const uint4
 }
 
 // Element index of (slot, KV head h, element d) in the cache
-// [num_blocks, Hkv, 16, D]: block slot / 16, offset slot % 16.
-__device__ __forceinline__ int64_t cache_elem(int64_t slot, int h, int Hkv, int D, int d) {
-  return (((slot >> 4) * Hkv + h) * 16 + (slot & 15)) * D + d;
+// [num_blocks, Hkv, BS, D] with BS = 2^bs_log2: block slot / BS, offset slot % BS.
+__device__ __forceinline__ int64_t cache_elem(int64_t slot, int h, int Hkv, int D, int d,
+                                              int bs_log2) {
+  const int64_t bs = int64_t(1) << bs_log2;
+  return (((slot >> bs_log2) * Hkv + h) * bs + (slot & (bs - 1))) * D + d;
 }
 
 }  // namespace pkv

@@ -24,6 +24,7 @@ struct DecodeParams {
   float* ws_lse;              // [B * Hq, max_parts]    fp32 partition log2-sum-exp
   unsigned int* err;          // device error word
   int B, Hq, Hkv, G, max_blocks, num_blocks, max_seq_len;
+  int ppb_shift;              // log2(block_size / 16): 16-token pages per block
   int part, max_parts;        // partition size (tokens) and partitions per sequence
   float qk_scale_log2;        // scale * log2(e)
 };
@@ -39,6 +40,7 @@ struct PrefillParams {
   float* out_lse;
   unsigned int* err;
   int num_seqs, Hq, Hkv, G, max_blocks, num_blocks, max_q_len, q_tile;
+  int ppb_shift;              // log2(block_size / 16)
   float qk_scale_log2;
 };
 
@@ -52,6 +54,7 @@ struct CacheWriteParams {
   const float* v_scales;
   unsigned int* err;
   int num_tokens, Hkv, D, num_blocks;
+  int bs_log2;                // log2(block_size)
 };
 
 struct RopeCacheParams {
@@ -68,6 +71,7 @@ struct RopeCacheParams {
   unsigned int* err;
   int64_t max_position;
   int rot, neox, num_tokens, Hq, Hkv, D, num_blocks;
+  int bs_log2;                // log2(block_size)
 };
 
 // Each launcher validates nothing (the entry points do) and returns

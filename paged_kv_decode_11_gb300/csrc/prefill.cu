@@ -49,7 +49,7 @@ __global__ void __launch_bounds__((kPrefillConsumers + 1) * 32)
   const int q0 = p.cu_q_lens[n];
   const int L = p.cu_q_lens[n + 1] - q0;
   const int ctx = p.seq_lens[n];
-  if (L < 0 || L > ctx || ctx > p.max_blocks * kBS) {
+  if (L < 0 || L > ctx || ctx > ((p.max_blocks * kBS) << p.ppb_shift)) {
     if (threadIdx.x == 0 && qt == 0 && h == 0) atomicOr(p.err, PKV_DEVERR_QLEN);
     return;
   }
@@ -90,12 +90,13 @@ __global__ void __launch_bounds__((kPrefillConsumers + 1) * 32)
         mbar_arrive_expect_tx(&full_bar[st], npg * 2 * Geo::PAGE_BYTES);
         uint8_t* dst = basep + st * STAGE;
         for (int pg = 0; pg < npg; ++pg) {
-          int id = p.block_tables[(int64_t)n * p.max_blocks + pg0 + pg];
+          const int lp = pg0 + pg;                     // logical 16-token page
+          int id = p.block_tables[(int64_t)n * p.max_blocks + (lp >> p.ppb_shift)];
           if (id < 0 || id >= p.num_blocks) {
             atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
             id = 0;
           }
-          const int z = id * p.Hkv + h;
+          const int z = ((id * p.Hkv + h) << p.ppb_shift) + (lp & ((1 << p.ppb_shift) - 1));
 #pragma unroll
           for (int bx = 0; bx < Geo::NBOX; ++bx) {
             tma_load_3d(dst + pg * Geo::PAGE_BYTES + bx * Geo::BOX_BYTES, &tmK, &full_bar[st],

@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(256) rope_cache_kernel(const RopeCacheParams p
   }
   const int64_t slot = p.slots[t];
   if (slot < 0) return;
-  if (slot >= (int64_t)p.num_blocks * kBS) {
+  if (slot >= ((int64_t)p.num_blocks << p.bs_log2)) {
     if (r == nq) atomicOr(p.err, PKV_DEVERR_SLOT);
     return;
   }
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(256) rope_cache_kernel(const RopeCacheParams p
     const int h = r / per_head, j = r - h * per_head;
     const uint16_t* row = static_cast<const uint16_t*>(p.key) + (t * p.Hkv + h) * p.D;
     const float ks = TO_FP8 ? p.k_scales[h] : 1.f;
-    const int64_t base = cache_elem(slot, h, p.Hkv, p.D, 0);
+    const int64_t base = cache_elem(slot, h, p.Hkv, p.D, 0, p.bs_log2);
     if (j < R) {
       int oa, ob;
       const Pair8 y = rotate_item<BF16, NEOX>(row, cs, p.rot, j, oa, ob);
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(256) rope_cache_kernel(const RopeCacheParams p
   const int h = r / C8, off = 8 * (r - h * C8);
   const uint16_t* row = static_cast<const uint16_t*>(p.value) + (t * p.Hkv + h) * p.D;
   const float vs = TO_FP8 ? p.v_scales[h] : 1.f;
-  store_row8<BF16, TO_FP8>(p.v_cache, cache_elem(slot, h, p.Hkv, p.D, off),
+  store_row8<BF16, TO_FP8>(p.v_cache, cache_elem(slot, h, p.Hkv, p.D, off, p.bs_log2),
                            *reinterpret_cast<const uint4*>(row + off), vs);
 }
 

@@ -64,7 +64,9 @@ def _decode(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,want", [
-    (dict(D=96), UNSUPPORTED), (dict(BS=32), UNSUPPORTED), (dict(Hq=34, Hkv=2), UNSUPPORTED),
+    (dict(D=96), UNSUPPORTED), (dict(BS=8), UNSUPPORTED), (dict(BS=48), UNSUPPORTED),
+    (dict(BS=128), UNSUPPORTED), (dict(BS=32, B=0, out=None), OK),
+    (dict(BS=64, B=0, out=None), OK), (dict(Hq=34, Hkv=2), UNSUPPORTED),
     (dict(Hq=9, Hkv=2), INVALID), (dict(q_dtype=FP8, kv_dtype=FP8), UNSUPPORTED),
     (dict(q_dtype=F16, kv_dtype=BF16), UNSUPPORTED), (dict(part=24), INVALID),
     (dict(part=8192 + 16), INVALID), (dict(out=None), INVALID), (dict(bt=None), INVALID),
@@ -150,7 +152,7 @@ def _rope(lib, **kw):
     (dict(rot=0), INVALID), (dict(rot=24), INVALID), (dict(rot=144), INVALID),
     (dict(D=64, rot=128), INVALID), (dict(maxpos=0), INVALID), (dict(pos=None), INVALID),
     (dict(cs=None), INVALID), (dict(cs=FAKE + 8), INVALID), (dict(q=None), INVALID),
-    (dict(ks=None), INVALID), (dict(src=FP8), UNSUPPORTED), (dict(BS=32), UNSUPPORTED),
+    (dict(ks=None), INVALID), (dict(src=FP8), UNSUPPORTED), (dict(BS=24), UNSUPPORTED),
     (dict(T=0, q=None, k=None), OK), (dict(Hq=0), INVALID),
 ])
 def test_rope_cache_argument_checks(lib, kw, want):
