@@ -50,8 +50,13 @@
  *    Logical token j of sequence b lives in physical block
  *    block_tables[b][j / BS] at offset j % BS. Query head h reads KV head
  *    h / G. Within a block each KV head's BS x D run is contiguous; the
- *    kernels read it as BS / 16 consecutive pages of 16 tokens.
- *  - Supported: D in {64, 128}; BS in {16, 32, 64}; G <= 16; q dtype F16 or BF16; KV
+ *    kernels read it as BS / 16 consecutive pages of 16 tokens, or gather a
+ *    16-token page row by row when BS < 16 (BS = 1 is token-level paging).
+ *  - Cache slots past a sequence's context (the rest of its last block) may
+ *    hold anything, NaN included: they are read with weight 0 and their
+ *    values are zeroed before they meet that weight.
+ *  - Supported: D in {64, 128}; BS a power of two from 1 to 64 (decode and
+ *    the cache writes; prefill needs BS >= 16); G <= 16; q dtype F16 or BF16; KV
  *    dtype equal to the q dtype, or FP8_E4M3 with per-KV-head fp32 scales
  *    (dequantised value = code * scale).
  */

@@ -76,15 +76,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // Tensor map {D, 16, num_blocks * Hkv} over a cache [num_blocks, Hkv, 16, D]:
 // one box is 16 page rows by min(row bytes, 128) bytes, swizzled so that
 // the fragment loads of the kernels are bank-conflict free.
-// log2 of the 16-token pages in a block of `block_size` tokens (16, 32 or 64),
-// or -1 for a size the kernels do not take.
+// log2 of a block size the kernels take (1, 2, 4, ..., 64), or -1.
+int block_log2(int block_size) {
+  for (int k = 0; k <= 6; ++k)
+    if (block_size == (1 << k)) return k;
+  return -1;
+}
+
+// log2 of the 16-token pages in a block (0 for blocks smaller than a page).
 int page_shift(int block_size) {
-  return block_size == 16 ? 0 : block_size == 32 ? 1 : block_size == 64 ? 2 : -1;
+  const int k = block_log2(block_size);
+  return k > 4 ? k - 4 : 0;
 }
 
 // Page rows and per-sequence token counts stay within int32.
-bool page_rows_fit(int num_blocks, int Hkv, int shift, int max_blocks_per_seq, int block_size) {
-  return (((int64_t)num_blocks * Hkv) << shift) < ((int64_t)1 << 31) &&
+bool page_rows_fit(int num_blocks, int Hkv, int block_size, int max_blocks_per_seq) {
+  return (int64_t)num_blocks * Hkv * block_size < ((int64_t)1 << 31) &&
          (int64_t)max_blocks_per_seq * block_size < ((int64_t)1 << 30);
 }
 
@@ -188,10 +195,13 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const 
     return PKV_ERR_INVALID_ARG;
   if (!valid_dtypes(q_dtype, kv_dtype)) return PKV_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  const int bs_log2 = block_log2(block_size);
+  if (bs_log2 < 0) return PKV_ERR_UNSUPPORTED;
   const int shift = page_shift(block_size);
-  if (shift < 0) return PKV_ERR_UNSUPPORTED;
-  if (!page_rows_fit(num_blocks, num_kv_heads, shift, max_blocks_per_seq, block_size))
+  if (!page_rows_fit(num_blocks, num_kv_heads, block_size, max_blocks_per_seq))
     return PKV_ERR_INVALID_ARG;
+  // blocks below a page are gathered per token, with at most this many per partition
+  if (bs_log2 < 4 && partition_tokens > kGatherMaxPartitionTokens) return PKV_ERR_UNSUPPORTED;
   const int G = num_q_heads / num_kv_heads;
   if (G > 16) return PKV_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
@@ -208,9 +218,10 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const 
   if (workspace == nullptr || workspace_bytes < pl.bytes ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return PKV_ERR_WORKSPACE;
-  CUtensorMap tmK, tmV;
-  if (!make_kv_tmap(&tmK, k_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift) ||
-      !make_kv_tmap(&tmV, v_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift))
+  CUtensorMap tmK{}, tmV{};
+  if (bs_log2 >= 4 &&
+      (!make_kv_tmap(&tmK, k_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift) ||
+       !make_kv_tmap(&tmV, v_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift)))
     return PKV_ERR_CUDA;
   unsigned int* err = err_word();
   if (err == nullptr) return PKV_ERR_CUDA;
@@ -222,6 +233,8 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const 
   DecodeParams p{};
   p.out = out;
   p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
   p.block_tables = block_tables;
   p.seq_lens = seq_lens;
   p.k_scales = k_scales;
@@ -239,6 +252,7 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const 
   p.num_blocks = num_blocks;
   p.max_seq_len = max_seq_len;
   p.ppb_shift = shift;
+  p.bs_log2 = bs_log2;
   p.part = pl.part;
   p.max_parts = pl.max_parts;
   p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
@@ -260,9 +274,10 @@ pkv_status paged_attn_prefill_chunk(void* out, const void* q, pkv_dtype q_dtype,
   if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   if (!valid_dtypes(q_dtype, kv_dtype)) return PKV_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  const int bs_log2 = block_log2(block_size);
+  if (bs_log2 < 4) return PKV_ERR_UNSUPPORTED;
   const int shift = page_shift(block_size);
-  if (shift < 0) return PKV_ERR_UNSUPPORTED;
-  if (!page_rows_fit(num_blocks, num_kv_heads, shift, max_blocks_per_seq, block_size))
+  if (!page_rows_fit(num_blocks, num_kv_heads, block_size, max_blocks_per_seq))
     return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / num_kv_heads;
   if (G > 16) return PKV_ERR_UNSUPPORTED;
@@ -311,8 +326,8 @@ pkv_status reshape_and_cache(const void* key, const void* value, pkv_dtype src_d
   if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
   if (!valid_dtypes(src_dtype, kv_dtype)) return PKV_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  const int shift = page_shift(block_size);
-  if (shift < 0) return PKV_ERR_UNSUPPORTED;
+  const int bs_log2 = block_log2(block_size);
+  if (bs_log2 < 0) return PKV_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PKV_OK;
   if (!key || !value || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
   if (kv_dtype == PKV_FP8_E4M3 && (!k_scales || !v_scales)) return PKV_ERR_INVALID_ARG;
@@ -333,7 +348,7 @@ pkv_status reshape_and_cache(const void* key, const void* value, pkv_dtype src_d
   p.Hkv = num_kv_heads;
   p.D = head_dim;
   p.num_blocks = num_blocks;
-  p.bs_log2 = 4 + shift;
+  p.bs_log2 = bs_log2;
   return launch_cache_write(p, src_dtype, kv_dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -350,8 +365,8 @@ pkv_status rope_reshape_and_cache(void* query, const void* key, const void* valu
     return PKV_ERR_INVALID_ARG;
   if (!valid_dtypes(src_dtype, kv_dtype)) return PKV_ERR_UNSUPPORTED;
   if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
-  const int shift = page_shift(block_size);
-  if (shift < 0) return PKV_ERR_UNSUPPORTED;
+  const int bs_log2 = block_log2(block_size);
+  if (bs_log2 < 0) return PKV_ERR_UNSUPPORTED;
   if (rot_dim < 16 || rot_dim > head_dim || rot_dim % 16 != 0) return PKV_ERR_INVALID_ARG;
   if (num_tokens == 0) return PKV_OK;
   if (!query || !key || !value || !k_cache || !v_cache || !slot_mapping || !positions ||
@@ -383,7 +398,7 @@ pkv_status rope_reshape_and_cache(void* query, const void* key, const void* valu
   p.Hkv = num_kv_heads;
   p.D = head_dim;
   p.num_blocks = num_blocks;
-  p.bs_log2 = 4 + shift;
+  p.bs_log2 = bs_log2;
   return launch_rope_cache(p, src_dtype, kv_dtype, reinterpret_cast<cudaStream_t>(stream));
 }
 

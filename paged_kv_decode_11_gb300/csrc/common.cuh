@@ -159,11 +159,20 @@ __device__ __forceinline__ void qk_page(float (&acc)[NJ][4], int j0,
   }
 }
 
+// Zero mask of the 16-bit half of a packed pair holding token t, if t is not
+// among the page's first `valid` tokens (low half = even token).
+__device__ __forceinline__ uint32_t keep_pair(int t_even, int valid) {
+  return (t_even < valid ? 0x0000FFFFu : 0u) | (t_even + 1 < valid ? 0xFFFF0000u : 0u);
+}
+
 // oacc[t][.] += P . V_page for the page at shared-memory byte address vpage;
-// pa is the A fragment of P (16 rows x 16 tokens of this page).
+// pa is the A fragment of P (16 rows x 16 tokens of this page). Only the first
+// `valid` token rows of the page are real: the others get weight 0 in P, and
+// their V values are zeroed here so whatever the cache holds there (even NaN)
+// cannot reach the output.
 template <int D, int KV>
 __device__ __forceinline__ void pv_page(float (&oacc)[D / 8][4], const uint32_t (&pa)[4],
-                                        uint32_t vpage, int lane) {
+                                        uint32_t vpage, int lane, int valid = kBS) {
   using Geo = PageGeom<D, KV>;
   if constexpr (KV == KV_E4M3) {
     const int g = lane >> 2, c = lane & 3;
@@ -190,6 +199,15 @@ __device__ __forceinline__ void pv_page(float (&oacc)[D / 8][4], const uint32_t 
       wc[0] = cc.x; wc[1] = cc.y;
       wd[0] = d.x; wd[1] = d.y;
     }
+    if (valid < kBS) {
+#pragma unroll
+      for (int i = 0; i < CH / 4; ++i) {
+        if (t0 >= valid) wa[i] = 0u;
+        if (t1 >= valid) wb[i] = 0u;
+        if (8 + t0 >= valid) wc[i] = 0u;
+        if (8 + t1 >= valid) wd[i] = 0u;
+      }
+    }
 #pragma unroll
     for (int i = 0; i < CH / 4; ++i) {
       const uint32_t lo01 = __byte_perm(wa[i], wb[i], 0x5140);
@@ -208,6 +226,14 @@ __device__ __forceinline__ void pv_page(float (&oacc)[D / 8][4], const uint32_t 
     for (int t2 = 0; t2 < D / 16; ++t2) {
       uint32_t r[4];
       ldmatrix_x4_trans(r, vpage + Geo::elem_off(tok, 16 * t2 + 8 * (lane >> 4)));
+      if (valid < kBS) {
+        // r[0], r[2]: tokens 2c, 2c+1; r[1], r[3]: tokens 8+2c, 9+2c
+        const int c2 = 2 * (lane & 3);
+        r[0] &= keep_pair(c2, valid);
+        r[2] &= keep_pair(c2, valid);
+        r[1] &= keep_pair(8 + c2, valid);
+        r[3] &= keep_pair(8 + c2, valid);
+      }
       mma16816<BF>(oacc[2 * t2], pa, r[0], r[1]);
       mma16816<BF>(oacc[2 * t2 + 1], pa, r[2], r[3]);
     }

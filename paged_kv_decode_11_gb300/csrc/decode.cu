@@ -1,368 +1,10 @@
 // decode.cu — paged-KV decode attention: split-KV partitions and their
-// log-sum-exp merge in one kernel launch.
-//
-// Follows "flash attention decode (online softmax, paged KV, GQA)" and
-// "Split-KV paged attention for long context" (rvLLM: High-performance LLM
-// inference in Rust, Kernel Compiler Stack; Tier 2: Hand-written CUDA
-// kernels; FA3 v3 Attention Kernel, "split-KV ... distributes KV tiles across
-// thread blocks") and the log-sum-exp merge of partial attention (rapid_llm
-// README, feature table, "Decode context parallelism").
-//
-// Work decomposition: one CTA per (partition, KV head, sequence); a
-// partition is `part` consecutive tokens of one context. The CTA's NW warps
-// take the partition's pages round-robin, and each warp runs its own NST-deep
-// ring of TMA loads (one K page + one V page per stage, completion on an
-// mbarrier), issued by the warp itself as soon as it has read a stage, so
-// every warp keeps its own stream of requests in flight. The GQA group's
-// query heads sit in the MMA N dimension (decode_frags.cuh), so each K/V byte
-// is read from HBM once per call. Each warp runs an online softmax in the
-// log2 domain; at the end the warps are merged through shared memory (the
-// ring's space, then free). A sequence with one partition is written out
-// directly. Otherwise the partition's normalised output and its log2-sum-exp
-// go to the workspace and a per-(sequence, KV head) counter is bumped; the
-// CTA whose bump completes the count merges the partitions:
-//   LSE = log2 sum_p 2^{lse_p},  out = v_scale * sum_p 2^{lse_p - LSE} o_p.
-#include <cuda.h>
-#include "decode_frags.cuh"
-#include "launch.h"
+// log-sum-exp merge in one kernel launch (the kernel is in decode_kernel.cuh).
+// Caches with blocks of 16, 32 or 64 tokens are read a page at a time by TMA;
+// smaller blocks go to the gather instantiation in decode_gather.cu.
+#include "decode_kernel.cuh"
 
 namespace pkv {
-
-template <int D, int KV, int NT, int NW, int NST>
-struct DecodeCfg {
-  using Geo = PageGeom<D, KV>;
-  static constexpr int STAGE_BYTES = 2 * Geo::PAGE_BYTES;
-  static constexpr int RING_BYTES = NW * NST * STAGE_BYTES;
-  static constexpr int OBUF_BYTES = NW * 8 * NT * D * 4;      // warp merge, aliases the ring
-  static constexpr int SMEM_BYTES =
-      1024 + (RING_BYTES > OBUF_BYTES ? RING_BYTES : OBUF_BYTES);
-};
-
-template <int D, int KV, bool QBF16, int NT, int NW, int NST>
-__global__ void __launch_bounds__(NW * 32)
-    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                  const DecodeParams p) {
-  using Geo = PageGeom<D, KV>;
-  using Cfg = DecodeCfg<D, KV, NT, NW, NST>;
-  constexpr int STAGE = Cfg::STAGE_BYTES;
-  constexpr int NH = 8 * NT;                       // head columns of the N dimension
-  constexpr int MAXP = kMaxPartitionTokens / kBS;
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t bars[NW][NST];
-  __shared__ float red_m[NW][NH];
-  __shared__ float red_l[NW][NH];
-  __shared__ int s_ids[MAXP];
-  __shared__ int s_last;
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, c = lane & 3;
-  const int part_idx = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int G = p.G;
-
-  int ctx = p.seq_lens[b];
-  const int cap = min(p.max_seq_len, (p.max_blocks * kBS) << p.ppb_shift);
-  if (ctx < 0 || ctx > cap) {
-    if (tid == 0 && part_idx == 0 && h == 0) atomicOr(p.err, PKV_DEVERR_SEQ_LEN);
-    ctx = ctx < 0 ? 0 : cap;
-  }
-  const int nparts = ctx > 0 ? (ctx + p.part - 1) / p.part : 1;
-  if (part_idx >= nparts) return;
-  const int tok0 = part_idx * p.part;
-  const int tok1 = min(ctx, tok0 + p.part);
-  const int npages = (tok1 - tok0 + kBS - 1) / kBS;
-  const int page0 = tok0 / kBS;
-
-  const uint32_t raw_base = smem_u32(smem_raw);
-  const uint32_t base = (raw_base + 1023u) & ~1023u;
-  uint8_t* basep = smem_raw + (base - raw_base);
-
-  // page rows of the tensor maps: a block of 16 << ppb_shift tokens holds that
-  // many consecutive 16-token pages per KV head
-  const int sub_mask = (1 << p.ppb_shift) - 1;
-  for (int i = tid; i < npages; i += NW * 32) {
-    const int pg = page0 + i;
-    int id = p.block_tables[(int64_t)b * p.max_blocks + (pg >> p.ppb_shift)];
-    if (id < 0 || id >= p.num_blocks) {
-      atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
-      id = 0;
-    }
-    s_ids[i] = ((id * p.Hkv + h) << p.ppb_shift) + (pg & sub_mask);
-  }
-  if (tid == 0) {
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
-#pragma unroll
-    for (int w = 0; w < NW; ++w)
-#pragma unroll
-      for (int s = 0; s < NST; ++s) mbar_init(&bars[w][s], 1);
-    fence_barrier_init();
-  }
-  __syncthreads();
-
-  // ---- per-warp TMA ring, issued by the warp's lane 0 -----------------------------
-  const uint32_t wbase = base + warp * NST * STAGE;
-  uint8_t* wbasep = basep + warp * NST * STAGE;
-  const int nmine = warp < npages ? (npages - warp + NW - 1) / NW : 0;
-  auto issue = [&](int k) {
-    const int st = k % NST;
-    uint64_t* bar = &bars[warp][st];
-    const int z = s_ids[warp + NW * k];
-    uint8_t* dst = wbasep + st * STAGE;
-    mbar_arrive_expect_tx(bar, STAGE);
-#pragma unroll
-    for (int bx = 0; bx < Geo::NBOX; ++bx) {
-      tma_load_3d(dst + bx * Geo::BOX_BYTES, &tmK, bar, bx * Geo::BOX_ELEMS, 0, z);
-      tma_load_3d(dst + Geo::PAGE_BYTES + bx * Geo::BOX_BYTES, &tmV, bar, bx * Geo::BOX_ELEMS, 0,
-                  z);
-    }
-  };
-  if (lane == 0)
-    for (int k = 0; k < NST && k < nmine; ++k) issue(k);
-  int issued = min(NST, nmine);
-
-  // ---- query fragments (heads in N), straight from global memory --------------------
-  const uint16_t* qb = static_cast<const uint16_t*>(p.q) + ((int64_t)b * p.Hq + h * G) * D;
-  uint32_t qf[NT][D / 16][2];
-  load_qT_frags<D, KV, QBF16, NT>(qf, qb, G, lane);
-
-  float oacc[NT][D / 16][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int t = 0; t < D / 16; ++t)
-      oacc[nt][t][0] = oacc[nt][t][1] = oacc[nt][t][2] = oacc[nt][t][3] = 0.f;
-  float m[NT][2], l[NT][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    m[nt][0] = m[nt][1] = -INFINITY;
-    l[nt][0] = l[nt][1] = 0.f;
-  }
-  const float sl2 = p.qk_scale_log2 * (KV == KV_E4M3 ? p.k_scales[h] : 1.f);
-  const int tk0 = st_row_token<KV>(g, 0), tk8 = st_row_token<KV>(g, 1);
-
-  for (int k = 0; k < nmine; ++k) {
-    const int st = k % NST;
-    bool ok = mbar_wait_bounded(&bars[warp][st], (k / NST) & 1);
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) {
-      if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
-      // let what this warp still has in flight land (bounded), then stop
-      for (int kk = k + 1; kk < issued; ++kk)
-        mbar_wait_bounded(&bars[warp][kk % NST], (kk / NST) & 1, 1u << 16);
-      break;
-    }
-    const uint32_t kpage = wbase + st * STAGE;
-    const uint32_t vpage = kpage + Geo::PAGE_BYTES;
-    float s[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-    // E4M3: take the page into registers and refill the stage at once, so the
-    // next load is in flight while this page's math runs.
-    E4M3PageRegs<D> pr;
-    if constexpr (KV == KV_E4M3) {
-      load_e4m3_page<D>(pr, kpage, vpage, lane);
-      __syncwarp();
-      if (lane == 0 && k + NST < nmine) {
-        fence_proxy_async_smem();
-        issue(k + NST);
-      }
-      kq_regs<D, NT>(s, qf, pr.k);
-    } else {
-      kq_page<D, KV, NT>(s, qf, kpage, lane);
-    }
-
-    const int tbase = tok0 + (warp + NW * k) * kBS;
-    const bool v0 = tbase + tk0 < tok1, v8 = tbase + tk8 < tok1;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float x0 = v0 ? s[nt][e] * sl2 : -INFINITY;
-        const float x8 = v8 ? s[nt][2 + e] * sl2 : -INFINITY;
-        const float mx = col_max8(fmaxf(x0, x8));
-        const float mn = fmaxf(m[nt][e], mx);
-        const float ms = (mn == -INFINITY) ? 0.f : mn;
-        const float alpha = exp2f(m[nt][e] - ms);
-        m[nt][e] = mn;
-        const float p0 = exp2f(x0 - ms), p8 = exp2f(x8 - ms);
-        l[nt][e] = l[nt][e] * alpha + p0 + p8;
-        s[nt][e] = p0;
-        s[nt][2 + e] = p8;
-#pragma unroll
-        for (int t = 0; t < D / 16; ++t) {
-          oacc[nt][t][e] *= alpha;
-          oacc[nt][t][2 + e] *= alpha;
-        }
-      }
-    uint32_t pb[NT][2];
-    pT_frags<KV, NT>(pb, s);
-    if constexpr (KV == KV_E4M3) {
-      vp_regs<D, NT>(oacc, pb, pr.v);
-    } else {
-      vp_page<D, KV, NT>(oacc, pb, vpage, lane);
-      __syncwarp();
-      if (lane == 0 && k + NST < nmine) {
-        fence_proxy_async_smem();
-        issue(k + NST);
-      }
-    }
-    issued = min(k + 1 + NST, nmine);
-  }
-
-  // ---- merge the warps of this CTA ----------------------------------------------------
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      l[nt][e] = col_sum8(l[nt][e]);
-      if (g == 0) {
-        red_m[warp][8 * nt + 2 * c + e] = m[nt][e];
-        red_l[warp][8 * nt + 2 * c + e] = l[nt][e];
-      }
-    }
-  __syncthreads();  // every warp is done with its ring: the ring's space is free
-  float* obuf = reinterpret_cast<float*>(basep);   // [NW][G][D]
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int hh = 8 * nt + 2 * c + e;
-      if (hh < G) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w][hh]);
-        const float f = (m[nt][e] == -INFINITY) ? 0.f : exp2f(m[nt][e] - M);
-        float* orow = obuf + (warp * G + hh) * D;
-#pragma unroll
-        for (int t = 0; t < D / 16; ++t) {
-          orow[ot_row_dim<D, KV>(t, g, 0)] = oacc[nt][t][e] * f;
-          orow[ot_row_dim<D, KV>(t, g, 1)] = oacc[nt][t][2 + e] * f;
-        }
-      }
-    }
-  __syncthreads();
-
-  const float vscale = (KV == KV_E4M3) ? p.v_scales[h] : 1.f;
-  const int64_t row0 = (int64_t)b * p.Hq + h * G;
-  for (int idx = tid; idx < G * (D / 2); idx += NW * 32) {
-    const int hh = idx / (D / 2), d = 2 * (idx % (D / 2));
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, red_m[w][hh]);
-    float L = 0.f, o0 = 0.f, o1 = 0.f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      if (red_m[w][hh] != -INFINITY) L += red_l[w][hh] * exp2f(red_m[w][hh] - M);
-      o0 += obuf[(w * G + hh) * D + d];
-      o1 += obuf[(w * G + hh) * D + d + 1];
-    }
-    const bool nonempty = L > 0.f;
-    const float inv = nonempty ? 1.f / L : 0.f;
-    if (nparts == 1) {
-      *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + (row0 + hh) * D + d) =
-          pack2<QBF16>(o0 * inv * vscale, o1 * inv * vscale);
-      if (d == 0 && p.out_lse != nullptr)
-        p.out_lse[row0 + hh] = nonempty ? (M + log2f(L)) * kLn2 : -INFINITY;
-    } else {
-      const int64_t wrow = (row0 + hh) * p.max_parts + part_idx;
-      *reinterpret_cast<float2*>(p.ws_o + wrow * D + d) = make_float2(o0 * inv, o1 * inv);
-      if (d == 0) p.ws_lse[wrow] = nonempty ? M + log2f(L) : -INFINITY;
-    }
-  }
-  if (nparts == 1) return;
-
-  // ---- the CTA that completes the last partition of (b, h) merges them ------------------
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const unsigned long long before = atomicAdd(p.done + (int64_t)b * p.Hkv + h, 1ull);
-    s_last = (before + 1 == (unsigned long long)nparts);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  // The warps split the partitions; each lane owns D/32 dims of every head.
-  // Pass 1: the largest log2-sum-exp of each head.
-  constexpr int PER = D / 32;
-  float* mbuf = red_m[0];                         // [G] maxima (G <= NH)
-  for (int hh = warp; hh < G; hh += NW) {
-    const float* lse = p.ws_lse + (row0 + hh) * p.max_parts;
-    float mx = -INFINITY;
-    for (int s2 = lane; s2 < nparts; s2 += 32) mx = fmaxf(mx, ldcg_f32(lse + s2));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) mbuf[hh] = mx;
-  }
-  __syncthreads();
-  // Pass 2: weighted sums, four heads at a time, partitions round-robin over warps.
-  for (int h0 = 0; h0 < G; h0 += 4) {
-    const int nh = min(4, G - h0);
-    float acc[4][PER], z[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      z[j] = 0.f;
-#pragma unroll
-      for (int i = 0; i < PER; ++i) acc[j][i] = 0.f;
-    }
-#pragma unroll 4
-    for (int s2 = warp; s2 < nparts; s2 += NW) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (j >= nh) continue;
-        const int64_t wrow = (row0 + h0 + j) * p.max_parts + s2;
-        const float M = mbuf[h0 + j];
-        const float ls = ldcg_f32(p.ws_lse + wrow);
-        const float w = (ls == -INFINITY || M == -INFINITY) ? 0.f : exp2f(ls - M);
-        z[j] += w;
-        const float* o = p.ws_o + wrow * D + lane * PER;
-        if constexpr (PER == 4) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(o));
-          acc[j][0] += w * v.x; acc[j][1] += w * v.y; acc[j][2] += w * v.z; acc[j][3] += w * v.w;
-        } else {
-          const float2 v = __ldcg(reinterpret_cast<const float2*>(o));
-          acc[j][0] += w * v.x; acc[j][1] += w * v.y;
-        }
-      }
-    }
-    // combine the warps through shared memory (the ring's space is free)
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (j >= nh) break;
-#pragma unroll
-      for (int i = 0; i < PER; ++i) obuf[(warp * 4 + j) * D + lane * PER + i] = acc[j][i];
-      if (lane == 0) red_l[warp][j] = z[j];
-    }
-    __syncthreads();
-    for (int idx = tid; idx < nh * (D / 2); idx += NW * 32) {
-      const int j = idx / (D / 2), d = 2 * (idx % (D / 2));
-      float Z = 0.f, o0 = 0.f, o1 = 0.f;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        Z += red_l[w][j];
-        o0 += obuf[(w * 4 + j) * D + d];
-        o1 += obuf[(w * 4 + j) * D + d + 1];
-      }
-      const float inv = Z > 0.f ? vscale / Z : 0.f;
-      const int hh = h0 + j;
-      *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + (row0 + hh) * D + d) =
-          pack2<QBF16>(o0 * inv, o1 * inv);
-      if (d == 0 && p.out_lse != nullptr)
-        p.out_lse[row0 + hh] = Z > 0.f ? (mbuf[hh] + log2f(Z)) * kLn2 : -INFINITY;
-    }
-  }
-}
-
-// Warps per CTA and TMA ring depth per warp (E4M3 / 16-bit caches).
-#ifndef PKV_DECODE_NW
-#define PKV_DECODE_NW 4
-#endif
-#ifndef PKV_DECODE_NST_E4M3
-#define PKV_DECODE_NST_E4M3 3
-#endif
-#ifndef PKV_DECODE_NST_16
-#define PKV_DECODE_NST_16 2
-#endif
 
 size_t decode_smem_bytes(int head_dim, pkv_dtype kv_dtype, int G) {
   constexpr int NW = PKV_DECODE_NW;
@@ -374,51 +16,11 @@ size_t decode_smem_bytes(int head_dim, pkv_dtype kv_dtype, int G) {
   return 1024 + (ring > obuf ? ring : obuf);
 }
 
-template <int D, int KV, bool QBF16, int NT>
-static pkv_status launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK,
-                                  const CUtensorMap& tmV, cudaStream_t stream) {
-  constexpr int NW = PKV_DECODE_NW;
-  constexpr int NST = (KV == KV_E4M3) ? PKV_DECODE_NST_E4M3 : PKV_DECODE_NST_16;
-  using Cfg = DecodeCfg<D, KV, NT, NW, NST>;
-  auto kern = decode_kernel<D, KV, QBF16, NT, NW, NST>;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
-  static bool attr_set[64] = {};
-  if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg::SMEM_BYTES) != cudaSuccess)
-      return PKV_ERR_CUDA;
-    attr_set[dev] = true;
-  }
-  dim3 grid(p.max_parts, p.Hkv, p.B);
-  kern<<<grid, NW * 32, Cfg::SMEM_BYTES, stream>>>(tmK, tmV, p);
-  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
-}
-
-template <int D, int KV, bool QBF16>
-static pkv_status launch_decode_nt(const DecodeParams& p, const CUtensorMap& tmK,
-                                   const CUtensorMap& tmV, cudaStream_t stream) {
-  if (p.G > 8) return launch_decode_t<D, KV, QBF16, 2>(p, tmK, tmV, stream);
-  return launch_decode_t<D, KV, QBF16, 1>(p, tmK, tmV, stream);
-}
-
-template <int D>
-static pkv_status launch_decode_d(const DecodeParams& p, pkv_dtype q_dtype, pkv_dtype kv_dtype,
-                                  const CUtensorMap& tmK, const CUtensorMap& tmV,
-                                  cudaStream_t stream) {
-  const bool qbf = (q_dtype == PKV_BF16);
-  if (kv_dtype == PKV_FP8_E4M3)
-    return qbf ? launch_decode_nt<D, KV_E4M3, true>(p, tmK, tmV, stream)
-               : launch_decode_nt<D, KV_E4M3, false>(p, tmK, tmV, stream);
-  if (kv_dtype == PKV_BF16) return launch_decode_nt<D, KV_BF16, true>(p, tmK, tmV, stream);
-  return launch_decode_nt<D, KV_F16, false>(p, tmK, tmV, stream);
-}
-
 pkv_status launch_decode(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                          pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
                          cudaStream_t stream) {
-  if (head_dim == 128) return launch_decode_d<128>(p, q_dtype, kv_dtype, tmK, tmV, stream);
-  return launch_decode_d<64>(p, q_dtype, kv_dtype, tmK, tmV, stream);
+  if (p.bs_log2 < 4) return launch_decode_gather(p, head_dim, q_dtype, kv_dtype, stream);
+  return launch_decode_mode<false>(p, head_dim, q_dtype, kv_dtype, tmK, tmV, stream);
 }
 
 }  // namespace pkv

@@ -8,12 +8,17 @@
 
 namespace pkv {
 
-constexpr int kMaxPartitionTokens = 8192;   // split-KV partition cap (block ids staged in smem)
+constexpr int kMaxPartitionTokens = 8192;
+// Largest partition of the gather path (it keeps one cache row per token in
+// shared memory).
+constexpr int kGatherMaxPartitionTokens = 2048;   // split-KV partition cap (block ids staged in smem)
 constexpr int kDecodeWorkers = 4;           // resident decode CTAs per SM assumed by the planner
 
 struct DecodeParams {
   void* out;
   const void* q;
+  const void* k_cache;        // read directly only by the gather instantiation
+  const void* v_cache;
   const int32_t* block_tables;
   const int32_t* seq_lens;
   const float* k_scales;
@@ -24,7 +29,8 @@ struct DecodeParams {
   float* ws_lse;              // [B * Hq, max_parts]    fp32 partition log2-sum-exp
   unsigned int* err;          // device error word
   int B, Hq, Hkv, G, max_blocks, num_blocks, max_seq_len;
-  int ppb_shift;              // log2(block_size / 16): 16-token pages per block
+  int ppb_shift;              // log2(block_size / 16): 16-token pages per block (TMA mode)
+  int bs_log2;                // log2(block_size)
   int part, max_parts;        // partition size (tokens) and partitions per sequence
   float qk_scale_log2;        // scale * log2(e)
 };
@@ -79,6 +85,9 @@ struct RopeCacheParams {
 pkv_status launch_decode(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                          pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
                          cudaStream_t stream);
+// Decode for blocks of fewer than 16 tokens (pages gathered row by row).
+pkv_status launch_decode_gather(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
+                                pkv_dtype kv_dtype, cudaStream_t stream);
 // Dynamic shared memory of one decode CTA.
 size_t decode_smem_bytes(int head_dim, pkv_dtype kv_dtype, int G);
 pkv_status launch_prefill(const PrefillParams& p, int head_dim, pkv_dtype q_dtype,

@@ -202,7 +202,8 @@ __global__ void __launch_bounds__((kPrefillConsumers + 1) * 32)
         if (pg < npg && kbase + pg * kBS <= warp_lim) {
           uint32_t pa[4];
           pack_p<KV>(pa, s, 2 * pg);
-          pv_page<D, KV>(oacc, pa, vst + pg * Geo::PAGE_BYTES, lane);
+          pv_page<D, KV>(oacc, pa, vst + pg * Geo::PAGE_BYTES, lane,
+                         min(kBS, ctx - (kbase + pg * kBS)));
         }
       }
     }

@@ -64,7 +64,9 @@ def _decode(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,want", [
-    (dict(D=96), UNSUPPORTED), (dict(BS=8), UNSUPPORTED), (dict(BS=48), UNSUPPORTED),
+    (dict(D=96), UNSUPPORTED), (dict(BS=3), UNSUPPORTED), (dict(BS=48), UNSUPPORTED),
+    (dict(BS=1, B=0, out=None), OK), (dict(BS=8, B=0, out=None), OK),
+    (dict(BS=1, part=4096), UNSUPPORTED), (dict(BS=16, part=4096, B=0, out=None), OK),
     (dict(BS=128), UNSUPPORTED), (dict(BS=32, B=0, out=None), OK),
     (dict(BS=64, B=0, out=None), OK), (dict(Hq=34, Hkv=2), UNSUPPORTED),
     (dict(Hq=9, Hkv=2), INVALID), (dict(q_dtype=FP8, kv_dtype=FP8), UNSUPPORTED),

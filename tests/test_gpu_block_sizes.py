@@ -95,7 +95,7 @@ def test_prefill_vs_oracle(BS, L, P_, kv):
     assert_close(lse, wlse, LSE_TOL, f"BS{BS} prefill lse")
 
 
-@pytest.mark.parametrize("BS", [32, 64])
+@pytest.mark.parametrize("BS", [1, 32, 64])
 def test_rope_cache_bit_exact(BS):
     c = _case(BS, "fp8")
     cs = rope_cos_sin(int(c.new_positions.max()) + 1, c.D, 10000.0)
@@ -124,3 +124,109 @@ def test_decode_flags_block_id_past_pool_with_block_size_32():
     bt[5, 0] = c.num_blocks                            # one past the pool
     out, _ = run_decode(c, kc, vc, block_tables=bt)
     assert P.pkv_get_device_error() & 0x1
+
+
+# ---- blocks smaller than a page: rows gathered per token ------------------------------
+
+@pytest.mark.parametrize("BS", [1, 2, 8])
+@pytest.mark.parametrize("kv,dtype,Hq,Hkv,D", [("same", "bf16", 8, 2, 128),
+                                               ("fp8", "bf16", 32, 8, 128),
+                                               ("same", "f16", 12, 4, 64),
+                                               ("fp8", "f16", 16, 1, 64)])
+@pytest.mark.parametrize("part", [0, 48])
+def test_gather_decode_vs_oracle(BS, kv, dtype, Hq, Hkv, D, part):
+    c = _case(BS, kv, dtype, Hq, Hkv, D)
+    kc, vc = product_cache(c)
+    out, lse = run_decode(c, kc, vc, partition_tokens=part)
+    check_device_ok()
+    ko, vo = oracle_cache(c)
+    want, wlse = oracle_decode(c, ko, vo)
+    assert_close(out, want, tol(c), f"BS{BS} decode")
+    assert_close(lse, wlse, LSE_TOL, f"BS{BS} lse")
+
+
+@pytest.mark.parametrize("BS", [1, 8])
+@pytest.mark.parametrize("kv", ["same", "fp8"])
+def test_gather_cache_write_bit_exact(BS, kv):
+    c = _case(BS, kv)
+    kc, vc = product_cache(c)
+    torch.cuda.synchronize()
+    check_device_ok()
+    ko, vo = oracle_cache(c)
+    assert torch.equal(kc.cpu().view(torch.uint8), ko.view(torch.uint8))
+    assert torch.equal(vc.cpu().view(torch.uint8), vo.view(torch.uint8))
+
+
+@pytest.mark.parametrize("kv", ["same", "fp8"])
+def test_decode_bit_identical_from_token_blocks_to_page_blocks(kv):
+    outs = []
+    for BS in (1, 4, 16, 32):
+        c = _case(BS, kv, seed=24)
+        kc, vc = product_cache(c)
+        out, lse = run_decode(c, kc, vc, partition_tokens=64)
+        check_device_ok()
+        outs.append((out.cpu(), lse.cpu()))
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+
+
+def test_gather_decode_flags_bad_block_id():
+    c = _case(1)
+    kc, vc = product_cache(c)
+    bt = c.block_tables.copy()
+    bt[7, 3] = -2
+    run_decode(c, kc, vc, block_tables=bt)
+    assert P.pkv_get_device_error() & 0x1
+
+
+def test_prefill_refuses_blocks_below_a_page():
+    c = make_case("tiny", 25, B=2, BS=8, Hq=8, Hkv=2, D=128, dtype="bf16", kv="same",
+                  ctx=("fixed", [40, 70]), pool=("scale", 1.5), prefill=(20, 30))
+    kc, vc = product_cache(c)
+    with pytest.raises(P.PkvError):
+        run_prefill(c, kc, vc)
+
+
+# ---- slots past a context hold garbage: weight 0 must stay 0 ------------------------
+
+def _poison_tails(c, kc, vc):
+    ts = torch.as_tensor(c.tail_slots)
+    blk, off = (ts // c.BS).cuda(), (ts % c.BS).cuda()
+    if c.kv_fp8:
+        kc[blk, :, off, :] = 0x7F                       # E4M3 NaN
+        vc[blk, :, off, :] = 0x7F
+    else:
+        kc[blk, :, off, :] = float("nan")
+        vc[blk, :, off, :] = float("inf")
+    return len(c.tail_slots)
+
+
+@pytest.mark.parametrize("BS", [16, 32])
+@pytest.mark.parametrize("kv", ["same", "fp8"])
+def test_decode_ignores_nan_past_the_context(BS, kv):
+    c = _case(BS, kv, seed=26)
+    kc, vc = product_cache(c)
+    assert _poison_tails(c, kc, vc) > 0
+    for part in (0, 16, 48):
+        out, lse = run_decode(c, kc, vc, partition_tokens=part)
+        check_device_ok()
+        assert torch.isfinite(out.float()).all()
+    ko, vo = oracle_cache(c)
+    want, _ = oracle_decode(c, ko, vo)
+    assert_close(out, want, tol(c), f"BS{BS} decode with poisoned tails")
+
+
+@pytest.mark.parametrize("kv", ["same", "fp8"])
+def test_prefill_ignores_nan_past_the_context(kv):
+    c = make_case("tiny", 27, B=2, BS=16, Hq=8, Hkv=2, D=128, dtype="bf16", kv=kv,
+                  ctx=("fixed", [40, 70]), pool=("scale", 1.5), prefill=(37, 50))
+    kc, vc = product_cache(c)
+    assert _poison_tails(c, kc, vc) > 0
+    out, lse = run_prefill(c, kc, vc)
+    check_device_ok()
+    assert torch.isfinite(out.float()).all()
+    ko, vo = oracle_cache(c)
+    pf = c.prefill
+    want, _ = O.prefill_chunk(pf.q, ko, vo, pf.block_tables, pf.seq_lens, pf.cu_q_lens,
+                              c.scale, c.k_scales, c.v_scales)
+    assert_close(out, want, tol(c), "prefill with poisoned tails")
