@@ -203,6 +203,45 @@ pkv_status paged_attn_prefill_chunk(void* out, const void* q,
                                     void* stream);
 
 /*
+ * paged_attn_varlen — attention for a whole continuous-batching step in one
+ * call: decode sequences and prefill chunks over the same paged cache
+ * ("Continuous batching" and "Chunked Prefill", Litellama, Features).
+ *   Sequences [0, num_decode_seqs) are decode sequences, one query row each:
+ *   q rows 0 .. num_decode_seqs-1. Sequences [num_decode_seqs, num_seqs) are
+ *   prefill chunks: query_start_loc int32 [num_seqs + 1] holds the first q row
+ *   of every sequence (query_start_loc[i] = i for the decode sequences) and
+ *   query_start_loc[num_seqs] = total_q_tokens.
+ *   q, out: [total_q_tokens, Hq, D]; out_lse (optional): fp32
+ *   [total_q_tokens, Hq]. block_tables [num_seqs, max_blocks_per_seq] and
+ *   seq_lens [num_seqs] as for decode and prefill (seq_lens include the new
+ *   tokens, already cached by reshape_and_cache).
+ *   Decode rows are computed exactly as paged_attn_decode computes them
+ *   (max_decode_seq_len bounds their seq_lens and sizes the split; the
+ *   workspace is paged_attn_decode_workspace_size(num_decode_seqs, Hq, Hkv,
+ *   D, max_decode_seq_len, partition_tokens) bytes), chunk rows exactly as
+ *   paged_attn_prefill_chunk computes them (max_q_len bounds every chunk).
+ *   Everything is enqueued on `stream`: the split-KV counter reset, the
+ *   prefill kernel, then the decode kernel launched as a programmatic
+ *   dependent of the prefill kernel, so decode CTAs start on the room the
+ *   prefill grid leaves instead of waiting for it to finish. Block sizes:
+ *   >= 16 when there are chunks.
+ */
+pkv_status paged_attn_varlen(void* out, const void* q, pkv_dtype q_dtype,
+                             const void* k_cache, const void* v_cache,
+                             pkv_dtype kv_dtype, const int32_t* block_tables,
+                             const int32_t* seq_lens,
+                             const int32_t* query_start_loc, int num_seqs,
+                             int num_decode_seqs, int total_q_tokens,
+                             int max_q_len, int max_decode_seq_len,
+                             int num_q_heads, int num_kv_heads, int head_dim,
+                             int block_size, int max_blocks_per_seq,
+                             int num_blocks, float scale,
+                             const float* k_scales, const float* v_scales,
+                             int partition_tokens, float* out_lse,
+                             void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/*
  * reshape_and_cache — write the K/V rows of new tokens into their slots.
  *   key, value: [num_tokens, Hkv, D] in src_dtype (F16 or BF16).
  *   slot_mapping: int64 [num_tokens]; slot s names block s / BS, offset

@@ -24,8 +24,8 @@ DEVERR_BITS = {0x1: "block id", 0x2: "slot", 0x4: "seq_len", 0x8: "timeout", 0x1
 
 # Every symbol include/pkv.h declares.
 EXPORTS = ("paged_attn_decode_workspace_size", "paged_attn_decode", "paged_attn_decode_noalloc",
-           "paged_attn_prefill_chunk", "reshape_and_cache", "rope_reshape_and_cache",
-           "pkv_get_device_error", "pkv_status_string")
+           "paged_attn_prefill_chunk", "paged_attn_varlen", "reshape_and_cache",
+           "rope_reshape_and_cache", "pkv_get_device_error", "pkv_status_string")
 
 _lib = None
 
@@ -60,6 +60,9 @@ def load(path: str = LIB_PATH):
     L.paged_attn_prefill_chunk.restype = I
     L.paged_attn_prefill_chunk.argtypes = [P, P, I, P, P, I, P, P, P, I, I, I, I, I, I, I, I, I,
                                            F, P, P, P, P]
+    L.paged_attn_varlen.restype = I
+    L.paged_attn_varlen.argtypes = [P, P, I, P, P, I, P, P, P, I, I, I, I, I, I, I, I, I, I, I, F,
+                                    P, P, I, P, P, S, P]
     L.reshape_and_cache.restype = I
     L.reshape_and_cache.argtypes = [P, P, I, P, P, I, P, I, I, I, I, I, P, P, P]
     L.rope_reshape_and_cache.restype = I
@@ -182,6 +185,38 @@ def paged_attn_prefill_chunk(out: torch.Tensor, q: torch.Tensor, k_cache: torch.
         Hq, hkv, D, bs, block_tables.shape[1], nb, float(scale), _dev_ptr(k_scales, "k_scales"),
         _dev_ptr(v_scales, "v_scales"), _dev_ptr(out_lse, "out_lse"), _stream(stream))
     _check("paged_attn_prefill_chunk", st)
+
+
+def paged_attn_varlen(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                      v_cache: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                      query_start_loc: torch.Tensor, num_decode_seqs: int, scale: float,
+                      max_q_len: int, max_decode_seq_len: int,
+                      k_scales: Optional[torch.Tensor] = None,
+                      v_scales: Optional[torch.Tensor] = None, partition_tokens: int = 0,
+                      out_lse: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """out[T, Hq, D] <- attention of a whole step: q rows 0..num_decode_seqs-1
+    are the decode sequences, the rest the prefill chunks that
+    query_start_loc [num_seqs + 1] delimits. One call, one stream."""
+    T, Hq, D = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    n = seq_lens.shape[0]
+    assert out.shape == q.shape and query_start_loc.shape[0] == n + 1
+    assert query_start_loc.dtype == torch.int32 and seq_lens.dtype == torch.int32
+    if workspace is None:
+        ws = paged_attn_decode_workspace_size(num_decode_seqs, Hq, hkv, D, max_decode_seq_len,
+                                              partition_tokens)
+        workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=q.device)
+    st = load().paged_attn_varlen(
+        _dev_ptr(out, "out"), _dev_ptr(q, "q"), dtype_code(q), _dev_ptr(k_cache, "k_cache"),
+        _dev_ptr(v_cache, "v_cache"), dtype_code(k_cache), _dev_ptr(block_tables, "block_tables"),
+        _dev_ptr(seq_lens, "seq_lens"), _dev_ptr(query_start_loc, "query_start_loc"), n,
+        int(num_decode_seqs), T, int(max_q_len), int(max_decode_seq_len), Hq, hkv, D, bs,
+        block_tables.shape[1], nb, float(scale), _dev_ptr(k_scales, "k_scales"),
+        _dev_ptr(v_scales, "v_scales"), int(partition_tokens), _dev_ptr(out_lse, "out_lse"),
+        _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    _check("paged_attn_varlen", st)
 
 
 def reshape_and_cache(key: torch.Tensor, value: torch.Tensor, k_cache: torch.Tensor,

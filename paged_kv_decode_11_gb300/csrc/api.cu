@@ -179,14 +179,30 @@ size_t paged_attn_decode_workspace_size(int num_seqs, int num_q_heads, int num_k
       .bytes;
 }
 
-pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const void* k_cache,
-                             const void* v_cache, pkv_dtype kv_dtype, const int32_t* block_tables,
-                             const int32_t* seq_lens, int num_seqs, int num_q_heads,
-                             int num_kv_heads, int head_dim, int block_size,
-                             int max_blocks_per_seq, int num_blocks, int max_seq_len, float scale,
-                             const float* k_scales, const float* v_scales, int partition_tokens,
-                             float* out_lse, void* workspace, size_t workspace_bytes,
-                             void* stream) {
+}  // extern "C"
+
+namespace {
+
+// A decode call checked and planned, ready to enqueue: the counter reset
+// (memset_bytes at p.done, 0 when a sequence has one partition at most) and
+// the kernel launch.
+struct DecodeCall {
+  DecodeParams p;
+  CUtensorMap tmK, tmV;
+  int head_dim;
+  pkv_dtype q_dtype, kv_dtype;
+  size_t memset_bytes;
+  bool empty;
+};
+
+pkv_status decode_setup(void* out, const void* q, pkv_dtype q_dtype, const void* k_cache,
+                        const void* v_cache, pkv_dtype kv_dtype, const int32_t* block_tables,
+                        const int32_t* seq_lens, int num_seqs, int num_q_heads, int num_kv_heads,
+                        int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+                        int max_seq_len, float scale, const float* k_scales,
+                        const float* v_scales, int partition_tokens, float* out_lse,
+                        void* workspace, size_t workspace_bytes, DecodeCall* call) {
+  call->empty = true;
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_seq_len < 0 ||
       max_blocks_per_seq <= 0 || num_blocks <= 0 || partition_tokens < 0)
     return PKV_ERR_INVALID_ARG;
@@ -206,6 +222,7 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const 
   if (G > 16) return PKV_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PKV_OK;
+  call->empty = false;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens)
     return PKV_ERR_INVALID_ARG;
   if (kv_dtype == PKV_FP8_E4M3 && (!k_scales || !v_scales)) return PKV_ERR_INVALID_ARG;
@@ -218,19 +235,22 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const 
   if (workspace == nullptr || workspace_bytes < pl.bytes ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return PKV_ERR_WORKSPACE;
-  CUtensorMap tmK{}, tmV{};
+  call->tmK = CUtensorMap{};
+  call->tmV = CUtensorMap{};
   if (bs_log2 >= 4 &&
-      (!make_kv_tmap(&tmK, k_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift) ||
-       !make_kv_tmap(&tmV, v_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift)))
+      (!make_kv_tmap(&call->tmK, k_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift) ||
+       !make_kv_tmap(&call->tmV, v_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift)))
     return PKV_ERR_CUDA;
   unsigned int* err = err_word();
   if (err == nullptr) return PKV_ERR_CUDA;
   char* ws = static_cast<char*>(workspace);
   // the partition counters start from zero in every call
-  if (pl.max_parts > 1 &&
-      cudaMemsetAsync(ws, 0, pl.off_o, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return PKV_ERR_CUDA;
-  DecodeParams p{};
+  call->memset_bytes = pl.max_parts > 1 ? pl.off_o : 0;
+  call->head_dim = head_dim;
+  call->q_dtype = q_dtype;
+  call->kv_dtype = kv_dtype;
+  DecodeParams& p = call->p;
+  p = DecodeParams{};
   p.out = out;
   p.q = q;
   p.k_cache = k_cache;
@@ -256,18 +276,38 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const 
   p.part = pl.part;
   p.max_parts = pl.max_parts;
   p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
-  return launch_decode(p, head_dim, q_dtype, kv_dtype, tmK, tmV,
-                       reinterpret_cast<cudaStream_t>(stream));
+  return PKV_OK;
 }
 
-pkv_status paged_attn_prefill_chunk(void* out, const void* q, pkv_dtype q_dtype,
-                                    const void* k_cache, const void* v_cache, pkv_dtype kv_dtype,
-                                    const int32_t* block_tables, const int32_t* seq_lens,
-                                    const int32_t* cu_q_lens, int num_seqs, int total_q_tokens,
-                                    int max_q_len, int num_q_heads, int num_kv_heads,
-                                    int head_dim, int block_size, int max_blocks_per_seq,
-                                    int num_blocks, float scale, const float* k_scales,
-                                    const float* v_scales, float* out_lse, void* stream) {
+pkv_status decode_reset(const DecodeCall& c, cudaStream_t stream) {
+  if (c.empty || c.memset_bytes == 0) return PKV_OK;
+  return cudaMemsetAsync(c.p.done, 0, c.memset_bytes, stream) == cudaSuccess ? PKV_OK
+                                                                            : PKV_ERR_CUDA;
+}
+
+pkv_status decode_launch(const DecodeCall& c, cudaStream_t stream, bool programmatic) {
+  if (c.empty) return PKV_OK;
+  return launch_decode(c.p, c.head_dim, c.q_dtype, c.kv_dtype, c.tmK, c.tmV, stream,
+                       programmatic);
+}
+
+
+struct PrefillCall {
+  PrefillParams p;
+  CUtensorMap tmK, tmV;
+  int head_dim;
+  pkv_dtype q_dtype, kv_dtype;
+  bool empty;
+};
+
+pkv_status prefill_setup(void* out, const void* q, pkv_dtype q_dtype, const void* k_cache,
+                         const void* v_cache, pkv_dtype kv_dtype, const int32_t* block_tables,
+                         const int32_t* seq_lens, const int32_t* cu_q_lens, int num_seqs,
+                         int total_q_tokens, int max_q_len, int num_q_heads, int num_kv_heads,
+                         int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+                         float scale, const float* k_scales, const float* v_scales,
+                         float* out_lse, PrefillCall* call) {
+  call->empty = true;
   if (num_seqs < 0 || total_q_tokens < 0 || max_q_len < 0 || num_q_heads <= 0 ||
       num_kv_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0)
     return PKV_ERR_INVALID_ARG;
@@ -283,18 +323,22 @@ pkv_status paged_attn_prefill_chunk(void* out, const void* q, pkv_dtype q_dtype,
   if (G > 16) return PKV_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q_tokens == 0 || max_q_len == 0) return PKV_OK;
+  call->empty = false;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !cu_q_lens)
     return PKV_ERR_INVALID_ARG;
   if (kv_dtype == PKV_FP8_E4M3 && (!k_scales || !v_scales)) return PKV_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PKV_ERR_INVALID_ARG;
-  CUtensorMap tmK, tmV;
-  if (!make_kv_tmap(&tmK, k_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift) ||
-      !make_kv_tmap(&tmV, v_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift))
+  if (!make_kv_tmap(&call->tmK, k_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift) ||
+      !make_kv_tmap(&call->tmV, v_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift))
     return PKV_ERR_CUDA;
   unsigned int* err = err_word();
   if (err == nullptr) return PKV_ERR_CUDA;
-  PrefillParams p{};
+  call->head_dim = head_dim;
+  call->q_dtype = q_dtype;
+  call->kv_dtype = kv_dtype;
+  PrefillParams& p = call->p;
+  p = PrefillParams{};
   p.out = out;
   p.q = q;
   p.block_tables = block_tables;
@@ -314,8 +358,99 @@ pkv_status paged_attn_prefill_chunk(void* out, const void* q, pkv_dtype q_dtype,
   p.q_tile = prefill_q_tile(G);
   p.ppb_shift = shift;
   p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
-  return launch_prefill(p, head_dim, q_dtype, kv_dtype, tmK, tmV,
-                        reinterpret_cast<cudaStream_t>(stream));
+  return PKV_OK;
+}
+
+pkv_status prefill_launch(const PrefillCall& c, cudaStream_t stream) {
+  if (c.empty) return PKV_OK;
+  return launch_prefill(c.p, c.head_dim, c.q_dtype, c.kv_dtype, c.tmK, c.tmV, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const void* k_cache,
+                             const void* v_cache, pkv_dtype kv_dtype, const int32_t* block_tables,
+                             const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                             int num_kv_heads, int head_dim, int block_size,
+                             int max_blocks_per_seq, int num_blocks, int max_seq_len, float scale,
+                             const float* k_scales, const float* v_scales, int partition_tokens,
+                             float* out_lse, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  DecodeCall c;
+  pkv_status st = decode_setup(out, q, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
+                               seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                               block_size, max_blocks_per_seq, num_blocks, max_seq_len, scale,
+                               k_scales, v_scales, partition_tokens, out_lse, workspace,
+                               workspace_bytes, &c);
+  if (st != PKV_OK || c.empty) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if ((st = decode_reset(c, s)) != PKV_OK) return st;
+  return decode_launch(c, s, false);
+}
+
+pkv_status paged_attn_prefill_chunk(void* out, const void* q, pkv_dtype q_dtype,
+                                    const void* k_cache, const void* v_cache, pkv_dtype kv_dtype,
+                                    const int32_t* block_tables, const int32_t* seq_lens,
+                                    const int32_t* cu_q_lens, int num_seqs, int total_q_tokens,
+                                    int max_q_len, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int block_size, int max_blocks_per_seq,
+                                    int num_blocks, float scale, const float* k_scales,
+                                    const float* v_scales, float* out_lse, void* stream) {
+  PrefillCall c;
+  pkv_status st = prefill_setup(out, q, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
+                                seq_lens, cu_q_lens, num_seqs, total_q_tokens, max_q_len,
+                                num_q_heads, num_kv_heads, head_dim, block_size,
+                                max_blocks_per_seq, num_blocks, scale, k_scales, v_scales,
+                                out_lse, &c);
+  if (st != PKV_OK || c.empty) return st;
+  return prefill_launch(c, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status paged_attn_varlen(void* out, const void* q, pkv_dtype q_dtype, const void* k_cache,
+                             const void* v_cache, pkv_dtype kv_dtype, const int32_t* block_tables,
+                             const int32_t* seq_lens, const int32_t* query_start_loc,
+                             int num_seqs, int num_decode_seqs, int total_q_tokens,
+                             int max_q_len, int max_decode_seq_len, int num_q_heads,
+                             int num_kv_heads, int head_dim, int block_size,
+                             int max_blocks_per_seq, int num_blocks, float scale,
+                             const float* k_scales, const float* v_scales, int partition_tokens,
+                             float* out_lse, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  if (num_seqs < 0 || num_decode_seqs < 0 || num_decode_seqs > num_seqs ||
+      total_q_tokens < num_decode_seqs || max_blocks_per_seq <= 0 || num_kv_heads <= 0)
+    return PKV_ERR_INVALID_ARG;
+  const int n_pf = num_seqs - num_decode_seqs;
+  if (n_pf > 0 && query_start_loc == nullptr) return PKV_ERR_INVALID_ARG;
+  if (!aligned16(out) || !aligned16(q)) return PKV_ERR_INVALID_ARG;
+  const int32_t* pf_tables = block_tables ? block_tables + (size_t)num_decode_seqs *
+                                                               max_blocks_per_seq
+                                          : nullptr;
+  DecodeCall dc;
+  PrefillCall pc;
+  pkv_status st = decode_setup(out, q, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
+                               seq_lens, num_decode_seqs, num_q_heads, num_kv_heads, head_dim,
+                               block_size, max_blocks_per_seq, num_blocks, max_decode_seq_len,
+                               scale, k_scales, v_scales, partition_tokens, out_lse, workspace,
+                               workspace_bytes, &dc);
+  if (st != PKV_OK) return st;
+  // the chunks' query rows follow the decode rows; their offsets in
+  // query_start_loc[num_decode_seqs ..] are absolute rows of q and out
+  st = prefill_setup(out, q, q_dtype, k_cache, v_cache, kv_dtype, pf_tables,
+                     seq_lens ? seq_lens + num_decode_seqs : nullptr,
+                     query_start_loc ? query_start_loc + num_decode_seqs : nullptr, n_pf,
+                     total_q_tokens - num_decode_seqs, max_q_len, num_q_heads, num_kv_heads,
+                     head_dim, block_size, max_blocks_per_seq, num_blocks, scale, k_scales,
+                     v_scales, out_lse, &pc);
+  if (st != PKV_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // counter reset, then the prefill chunks, then decode: decode is launched
+  // as a programmatic dependent of the prefill kernel, whose CTAs release it
+  // as they start, so both kinds of work share the GPU without a second stream
+  if ((st = decode_reset(dc, s)) != PKV_OK) return st;
+  if ((st = prefill_launch(pc, s)) != PKV_OK) return st;
+  return decode_launch(dc, s, !pc.empty);
 }
 
 pkv_status reshape_and_cache(const void* key, const void* value, pkv_dtype src_dtype,

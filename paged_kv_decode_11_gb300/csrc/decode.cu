@@ -18,9 +18,11 @@ size_t decode_smem_bytes(int head_dim, pkv_dtype kv_dtype, int G) {
 
 pkv_status launch_decode(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                          pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                         cudaStream_t stream) {
-  if (p.bs_log2 < 4) return launch_decode_gather(p, head_dim, q_dtype, kv_dtype, stream);
-  return launch_decode_mode<false>(p, head_dim, q_dtype, kv_dtype, tmK, tmV, stream);
+                         cudaStream_t stream, bool programmatic) {
+  if (p.bs_log2 < 4)
+    return launch_decode_gather(p, head_dim, q_dtype, kv_dtype, stream, programmatic);
+  return launch_decode_mode<false>(p, head_dim, q_dtype, kv_dtype, tmK, tmV, stream,
+                                   programmatic);
 }
 
 }  // namespace pkv

@@ -7,9 +7,10 @@
 namespace pkv {
 
 pkv_status launch_decode_gather(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
-                                pkv_dtype kv_dtype, cudaStream_t stream) {
+                                pkv_dtype kv_dtype, cudaStream_t stream, bool programmatic) {
   CUtensorMap unused{};
-  return launch_decode_mode<true>(p, head_dim, q_dtype, kv_dtype, unused, unused, stream);
+  return launch_decode_mode<true>(p, head_dim, q_dtype, kv_dtype, unused, unused, stream,
+                                  programmatic);
 }
 
 }  // namespace pkv

@@ -428,7 +428,8 @@ __global__ void __launch_bounds__(NW * 32)
 
 template <bool GATHER, int D, int KV, bool QBF16, int NT>
 static pkv_status launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK,
-                                  const CUtensorMap& tmV, cudaStream_t stream) {
+                                  const CUtensorMap& tmV, cudaStream_t stream,
+                                  bool programmatic) {
   constexpr int NW = PKV_DECODE_NW;
   constexpr int NST = (KV == KV_E4M3) ? PKV_DECODE_NST_E4M3 : PKV_DECODE_NST_16;
   using Cfg = DecodeCfg<D, KV, NT, NW, NST>;
@@ -443,35 +444,51 @@ static pkv_status launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK,
     attr_set[dev] = true;
   }
   dim3 grid(p.max_parts, p.Hkv, p.B);
+  if (programmatic) {
+    // may start while the previous kernel on the stream still runs (it
+    // reads nothing that kernel writes)
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(NW * 32);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tmK, tmV, p) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  }
   kern<<<grid, NW * 32, Cfg::SMEM_BYTES, stream>>>(tmK, tmV, p);
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 template <bool GATHER, int D, int KV, bool QBF16>
 static pkv_status launch_decode_nt(const DecodeParams& p, const CUtensorMap& tmK,
-                                   const CUtensorMap& tmV, cudaStream_t stream) {
-  if (p.G > 8) return launch_decode_t<GATHER, D, KV, QBF16, 2>(p, tmK, tmV, stream);
-  return launch_decode_t<GATHER, D, KV, QBF16, 1>(p, tmK, tmV, stream);
+                                   const CUtensorMap& tmV, cudaStream_t stream, bool prog) {
+  if (p.G > 8) return launch_decode_t<GATHER, D, KV, QBF16, 2>(p, tmK, tmV, stream, prog);
+  return launch_decode_t<GATHER, D, KV, QBF16, 1>(p, tmK, tmV, stream, prog);
 }
 
 template <bool GATHER, int D>
 static pkv_status launch_decode_d(const DecodeParams& p, pkv_dtype q_dtype, pkv_dtype kv_dtype,
                                   const CUtensorMap& tmK, const CUtensorMap& tmV,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, bool prog) {
   const bool qbf = (q_dtype == PKV_BF16);
   if (kv_dtype == PKV_FP8_E4M3)
-    return qbf ? launch_decode_nt<GATHER, D, KV_E4M3, true>(p, tmK, tmV, stream)
-               : launch_decode_nt<GATHER, D, KV_E4M3, false>(p, tmK, tmV, stream);
-  if (kv_dtype == PKV_BF16) return launch_decode_nt<GATHER, D, KV_BF16, true>(p, tmK, tmV, stream);
-  return launch_decode_nt<GATHER, D, KV_F16, false>(p, tmK, tmV, stream);
+    return qbf ? launch_decode_nt<GATHER, D, KV_E4M3, true>(p, tmK, tmV, stream, prog)
+               : launch_decode_nt<GATHER, D, KV_E4M3, false>(p, tmK, tmV, stream, prog);
+  if (kv_dtype == PKV_BF16)
+    return launch_decode_nt<GATHER, D, KV_BF16, true>(p, tmK, tmV, stream, prog);
+  return launch_decode_nt<GATHER, D, KV_F16, false>(p, tmK, tmV, stream, prog);
 }
 
 template <bool GATHER>
 pkv_status launch_decode_mode(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                               pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, bool prog) {
   if (head_dim == 128)
-    return launch_decode_d<GATHER, 128>(p, q_dtype, kv_dtype, tmK, tmV, stream);
-  return launch_decode_d<GATHER, 64>(p, q_dtype, kv_dtype, tmK, tmV, stream);
+    return launch_decode_d<GATHER, 128>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);
+  return launch_decode_d<GATHER, 64>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);
 }
 }  // namespace pkv

@@ -82,12 +82,14 @@ struct RopeCacheParams {
 
 // Each launcher validates nothing (the entry points do) and returns
 // PKV_ERR_CUDA on a launch failure.
+// programmatic: launch as a programmatic dependent of the previous kernel on
+// the stream (it may start once that kernel's CTAs have all signalled).
 pkv_status launch_decode(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                          pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                         cudaStream_t stream);
+                         cudaStream_t stream, bool programmatic = false);
 // Decode for blocks of fewer than 16 tokens (pages gathered row by row).
 pkv_status launch_decode_gather(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
-                                pkv_dtype kv_dtype, cudaStream_t stream);
+                                pkv_dtype kv_dtype, cudaStream_t stream, bool programmatic);
 // Dynamic shared memory of one decode CTA.
 size_t decode_smem_bytes(int head_dim, pkv_dtype kv_dtype, int G);
 pkv_status launch_prefill(const PrefillParams& p, int head_dim, pkv_dtype q_dtype,

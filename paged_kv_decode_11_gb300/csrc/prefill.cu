@@ -43,6 +43,9 @@ __global__ void __launch_bounds__((kPrefillConsumers + 1) * 32)
   __shared__ uint64_t full_bar[NST];
   __shared__ uint64_t empty_bar[NST];
 
+  // a decode launched behind this kernel as a programmatic dependent may take
+  // the SM room this grid leaves as soon as all of its CTAs are running
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int qt = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int G = p.G;

@@ -6,9 +6,10 @@ A decode step writes the new token of every sequence into its slot
 ("RoPE + KV cache write" followed by "Flash Attention Decode", rvLLM:
 High-performance LLM inference in Rust, Kernel Compiler Stack). A mixed
 step also carries a chunked-prefill chunk (Litellama, Features, "Chunked
-Prefill"): after one cache write of every new token, decode and the prefill
-chunk run on two streams, so the bandwidth-bound decode and the
-compute-bound prefill overlap on the GPU.
+Prefill"): after one cache write of every new token, the bandwidth-bound
+decode and the compute-bound prefill chunk overlap on the GPU, either
+through one paged_attn_varlen call on one stream or through the two entry
+points on two streams.
 """
 from __future__ import annotations
 
@@ -78,31 +79,60 @@ class DecodeStep:
 
 
 class MixedStep:
-    """Decode of many sequences plus one prefill chunk, sharing one cache."""
+    """Decode of many sequences plus one prefill chunk, sharing one cache.
+
+    mode "varlen" (default): one cache write of every new token, then one
+    paged_attn_varlen call over the whole batch (decode rows first, then the
+    chunk), which overlaps the two kinds of work on one stream. mode
+    "streams": the same two kernels through the separate entry points, the
+    chunk on a second stream."""
 
     def __init__(self, decode: DecodeStep, all_new_k, all_new_v, all_new_slots, pf_q,
-                 pf_block_tables, pf_seq_lens, pf_cu_q_lens, pf_max_q_len):
+                 pf_block_tables, pf_seq_lens, pf_cu_q_lens, pf_max_q_len, mode: str = "varlen"):
+        assert mode in ("varlen", "streams")
+        self.mode = mode
         self.decode = decode
         self.all_new_k, self.all_new_v, self.all_new_slots = all_new_k, all_new_v, all_new_slots
         self.pf_q = pf_q
         self.pf_block_tables, self.pf_seq_lens, self.pf_cu_q_lens = (pf_block_tables, pf_seq_lens,
                                                                      pf_cu_q_lens)
         self.pf_max_q_len = int(pf_max_q_len)
-        self.prefill_out = torch.empty_like(pf_q)
-        self.prefill_lse = torch.empty(pf_q.shape[:2], dtype=torch.float32, device=pf_q.device)
-        self.side = torch.cuda.Stream(device=pf_q.device)
-        self.ev_written = torch.cuda.Event()
-        self.ev_prefill = torch.cuda.Event()
+        d = decode
+        nd, L = d.q.shape[0], pf_q.shape[0]
+        dev = pf_q.device
+        if mode == "varlen":
+            # one batch: decode rows, then the chunk rows
+            self.q_all = torch.cat([d.q, pf_q]).contiguous()
+            self.out_all = torch.empty_like(self.q_all)
+            self.lse_all = torch.empty(self.q_all.shape[:2], dtype=torch.float32, device=dev)
+            width = max(d.block_tables.shape[1], pf_block_tables.shape[1])
+            bt = torch.zeros((nd + pf_block_tables.shape[0], width), dtype=torch.int32, device=dev)
+            bt[:nd, :d.block_tables.shape[1]] = d.block_tables
+            bt[nd:, :pf_block_tables.shape[1]] = pf_block_tables
+            self.bt_all = bt
+            self.seq_lens_all = torch.cat([d.seq_lens, pf_seq_lens]).contiguous()
+            self.qsl = torch.cat([torch.arange(nd, dtype=torch.int32, device=dev),
+                                  pf_cu_q_lens.to(torch.int32) + nd]).contiguous()
+            self.prefill_out = self.out_all[nd:]
+            self.prefill_lse = self.lse_all[nd:]
+        else:
+            self.prefill_out = torch.empty_like(pf_q)
+            self.prefill_lse = torch.empty(pf_q.shape[:2], dtype=torch.float32, device=dev)
+            self.side = torch.cuda.Stream(device=dev)
+            self.ev_written = torch.cuda.Event()
+            self.ev_prefill = torch.cuda.Event()
 
     @classmethod
-    def from_case(cls, case, k_cache, v_cache):
+    def from_case(cls, case, k_cache, v_cache, mode: str = "varlen"):
         d = DecodeStep.from_case(case, k_cache, v_cache)
         pf = case.prefill
         return cls(d, _dev(case.new_k), _dev(case.new_v), _dev(case.new_slots), _dev(pf.q),
-                   _dev(pf.block_tables), _dev(pf.seq_lens), _dev(pf.cu_q_lens), pf.L)
+                   _dev(pf.block_tables), _dev(pf.seq_lens), _dev(pf.cu_q_lens), pf.L, mode)
 
     @property
     def out(self):
+        if self.mode == "varlen":
+            return self.out_all[:self.decode.q.shape[0]]
         return self.decode.out
 
     def run(self, stream: Optional[torch.cuda.Stream] = None):
@@ -110,10 +140,16 @@ class MixedStep:
         d = self.decode
         B.reshape_and_cache(self.all_new_k, self.all_new_v, d.k_cache, d.v_cache,
                             self.all_new_slots, d.k_scales, d.v_scales, stream=main)
+        if self.mode == "varlen":
+            B.paged_attn_varlen(self.out_all, self.q_all, d.k_cache, d.v_cache, self.bt_all,
+                                self.seq_lens_all, self.qsl, d.q.shape[0], d.scale,
+                                self.pf_max_q_len, d.max_seq_len, d.k_scales, d.v_scales,
+                                partition_tokens=d.partition_tokens, out_lse=self.lse_all,
+                                workspace=d.workspace, stream=main)
+            return
         self.ev_written.record(main)
         self.side.wait_event(self.ev_written)
-        # prefill first: its CTAs take their SMs, and the persistent decode
-        # grid claims work on whatever room is left, then everywhere
+        # prefill first: its CTAs take their SMs, decode fills the rest
         B.paged_attn_prefill_chunk(self.prefill_out, self.pf_q, d.k_cache, d.v_cache,
                                    self.pf_block_tables, self.pf_seq_lens, self.pf_cu_q_lens,
                                    d.scale, self.pf_max_q_len, d.k_scales, d.v_scales,
@@ -124,8 +160,13 @@ class MixedStep:
 
     def inputs(self):
         d = self.decode
+        if self.mode == "varlen":
+            return [self.q_all, self.all_new_k, self.all_new_v, self.all_new_slots, self.bt_all,
+                    self.seq_lens_all, self.qsl]
         return [d.q, self.all_new_k, self.all_new_v, self.all_new_slots, d.block_tables,
                 d.seq_lens, self.pf_q, self.pf_block_tables, self.pf_seq_lens, self.pf_cu_q_lens]
 
     def outputs(self):
+        if self.mode == "varlen":
+            return [self.out_all]
         return [self.decode.out, self.prefill_out]

@@ -74,29 +74,37 @@ def test_decode_step_graph_replay_matches_eager(name):
     assert_close(replayed[torch.as_tensor(sel)], want, tol(c), f"{name} graph replay")
 
 
-def test_mixed_step_graph_replay_matches_eager():
+@pytest.mark.parametrize("mode", ["varlen", "streams"])
+def test_mixed_step_graph_replay_matches_eager(mode):
     from paged_kv_decode_11_gb300.step import MixedStep
     c = make_case("mixed", 0, device="cuda")
     kc, vc = product_cache(c, write_new=False)
-    step = MixedStep.from_case(c, kc, vc)
+    step = MixedStep.from_case(c, kc, vc, mode=mode)
     g = capture(step)
     d = step.decode
-    d.q.copy_(fresh_q(d.q, 21).cuda())
-    step.pf_q.copy_(fresh_q(step.pf_q, 22).cuda())
+    nd = d.q.shape[0]
+    q_new, pq_new = fresh_q(d.q, 21).cuda(), fresh_q(step.pf_q, 22).cuda()
+    if mode == "varlen":                       # the step reads its own batched copy
+        step.q_all[:nd].copy_(q_new)
+        step.q_all[nd:].copy_(pq_new)
+    else:
+        d.q.copy_(q_new)
+        step.pf_q.copy_(pq_new)
     g.replay()
     torch.cuda.synchronize()
-    rd, rp = d.out.clone(), step.prefill_out.clone()
+    rd, rp = step.out.clone(), step.prefill_out.clone()
     step.run()
     torch.cuda.synchronize()
     check_device_ok()
-    assert torch.equal(rd, d.out), "decode output of the replayed mixed step differs"
-    assert torch.equal(rp, step.prefill_out), "prefill output of the replayed mixed step differs"
+    as_bytes = lambda t: t.contiguous().view(torch.uint8)
+    assert torch.equal(as_bytes(rd), as_bytes(step.out)), "decode rows of the replay differ"
+    assert torch.equal(as_bytes(rp), as_bytes(step.prefill_out)), "chunk rows of the replay differ"
     # prefill of the replayed step against the oracle
     ko, vo = oracle_cache(c)
     pf = c.prefill
-    pw, _ = O.prefill_chunk(step.pf_q.cpu(), ko, vo, pf.block_tables, pf.seq_lens,
-                            pf.cu_q_lens, c.scale)
-    assert_close(rp, pw, tol(c), "mixed prefill (graph replay)")
+    pw, _ = O.prefill_chunk(pq_new.cpu(), ko, vo, pf.block_tables, pf.seq_lens, pf.cu_q_lens,
+                            c.scale)
+    assert_close(rp, pw, tol(c), f"mixed prefill (graph replay, {mode})")
 
 
 def test_graph_replays_are_deterministic():
