@@ -143,6 +143,9 @@ __global__ void __launch_bounds__(NW * 32)
   const int nmine = warp < npages ? (npages - warp + NW - 1) / NW : 0;
   const uint8_t* kcache = static_cast<const uint8_t*>(p.k_cache);
   const uint8_t* vcache = static_cast<const uint8_t*>(p.v_cache);
+  // KV pages are read once per call: mark them first to go from L2, so they
+  // do not push out what is reused (block tables, queries, partials)
+  const uint64_t evict_first = policy_evict_first();
   auto issue = [&](int k) {
     const int st = k % NST;
     uint64_t* bar = &bars[warp][st];
@@ -156,8 +159,8 @@ __global__ void __launch_bounds__(NW * 32)
         const uint32_t so = (x / Geo::BOX_ROW_BYTES) * Geo::BOX_BYTES +
                             Geo::swz(r, x % Geo::BOX_ROW_BYTES);
         const int64_t go = (int64_t)rows[r] * Geo::ROW_BYTES + x;
-        cp_async16(dst + so, kcache + go);
-        cp_async16(dst + Geo::PAGE_BYTES + so, vcache + go);
+        cp_async16_hint(dst + so, kcache + go, evict_first);
+        cp_async16_hint(dst + Geo::PAGE_BYTES + so, vcache + go, evict_first);
       }
       cp_async_mbar_arrive_noinc(bar);
     } else {
@@ -165,9 +168,10 @@ __global__ void __launch_bounds__(NW * 32)
       mbar_arrive_expect_tx(bar, STAGE);
 #pragma unroll
       for (int bx = 0; bx < Geo::NBOX; ++bx) {
-        tma_load_3d(dst + bx * Geo::BOX_BYTES, &tmK, bar, bx * Geo::BOX_ELEMS, 0, z);
-        tma_load_3d(dst + Geo::PAGE_BYTES + bx * Geo::BOX_BYTES, &tmV, bar, bx * Geo::BOX_ELEMS,
-                    0, z);
+        tma_load_3d_hint(dst + bx * Geo::BOX_BYTES, &tmK, bar, bx * Geo::BOX_ELEMS, 0, z,
+                         evict_first);
+        tma_load_3d_hint(dst + Geo::PAGE_BYTES + bx * Geo::BOX_BYTES, &tmV, bar,
+                         bx * Geo::BOX_ELEMS, 0, z, evict_first);
       }
     }
   };

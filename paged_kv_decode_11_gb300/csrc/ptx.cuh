@@ -89,6 +89,15 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
                : "memory");
 }
 
+// Same, with an L2 eviction-priority hint (policy from createpolicy).
+__device__ __forceinline__ void cp_async16_hint(void* smem_dst, const void* gsrc,
+                                                uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(
+                   smem_u32(smem_dst)),
+               "l"(gsrc), "l"(policy)
+               : "memory");
+}
+
 // The mbarrier receives one arrival once every cp.async this thread issued so
 // far has landed (the arrival counts toward the barrier's expected count).
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
