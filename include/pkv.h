@@ -55,8 +55,9 @@
  *  - Cache slots past a sequence's context (the rest of its last block) may
  *    hold anything, NaN included: they are read with weight 0 and their
  *    values are zeroed before they meet that weight.
- *  - Supported: D in {64, 128}; BS a power of two from 1 to 64 (decode and
- *    the cache writes; prefill needs BS >= 16); G <= 16; q dtype F16 or BF16; KV
+ *  - Supported: D in {64, 128, 256}; BS a power of two from 1 to 64 (decode
+ *    and the cache writes; prefill, and decode at D = 256, need BS >= 16);
+ *    G <= 16 (G <= 8 at D = 256); q dtype F16 or BF16; KV
  *    dtype equal to the q dtype, or FP8_E4M3 with per-KV-head fp32 scales
  *    (dequantised value = code * scale).
  */

@@ -210,16 +210,18 @@ pkv_status decode_setup(void* out, const void* q, pkv_dtype q_dtype, const void*
   if (partition_tokens % 16 != 0 || partition_tokens > kMaxPartitionTokens)
     return PKV_ERR_INVALID_ARG;
   if (!valid_dtypes(q_dtype, kv_dtype)) return PKV_ERR_UNSUPPORTED;
-  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PKV_ERR_UNSUPPORTED;
   const int bs_log2 = block_log2(block_size);
   if (bs_log2 < 0) return PKV_ERR_UNSUPPORTED;
   const int shift = page_shift(block_size);
   if (!page_rows_fit(num_blocks, num_kv_heads, block_size, max_blocks_per_seq))
     return PKV_ERR_INVALID_ARG;
-  // blocks below a page are gathered per token, with at most this many per partition
-  if (bs_log2 < 4 && partition_tokens > kGatherMaxPartitionTokens) return PKV_ERR_UNSUPPORTED;
+  // blocks below a page are gathered per token, with at most this many per
+  // partition and rows of at most 256 bytes
+  if (bs_log2 < 4 && (partition_tokens > kGatherMaxPartitionTokens || head_dim > 128))
+    return PKV_ERR_UNSUPPORTED;
   const int G = num_q_heads / num_kv_heads;
-  if (G > 16) return PKV_ERR_UNSUPPORTED;
+  if (G > 16 || (head_dim > 128 && G > 8)) return PKV_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PKV_OK;
   call->empty = false;
@@ -313,14 +315,14 @@ pkv_status prefill_setup(void* out, const void* q, pkv_dtype q_dtype, const void
     return PKV_ERR_INVALID_ARG;
   if (num_q_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
   if (!valid_dtypes(q_dtype, kv_dtype)) return PKV_ERR_UNSUPPORTED;
-  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PKV_ERR_UNSUPPORTED;
   const int bs_log2 = block_log2(block_size);
   if (bs_log2 < 4) return PKV_ERR_UNSUPPORTED;
   const int shift = page_shift(block_size);
   if (!page_rows_fit(num_blocks, num_kv_heads, block_size, max_blocks_per_seq))
     return PKV_ERR_INVALID_ARG;
   const int G = num_q_heads / num_kv_heads;
-  if (G > 16) return PKV_ERR_UNSUPPORTED;
+  if (G > 16 || (head_dim > 128 && G > 8)) return PKV_ERR_UNSUPPORTED;
   if (num_seqs > 65535 || num_kv_heads > 65535) return PKV_ERR_UNSUPPORTED;
   if (num_seqs == 0 || total_q_tokens == 0 || max_q_len == 0) return PKV_OK;
   call->empty = false;
@@ -460,7 +462,7 @@ pkv_status reshape_and_cache(const void* key, const void* value, pkv_dtype src_d
                              const float* k_scales, const float* v_scales, void* stream) {
   if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
   if (!valid_dtypes(src_dtype, kv_dtype)) return PKV_ERR_UNSUPPORTED;
-  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PKV_ERR_UNSUPPORTED;
   const int bs_log2 = block_log2(block_size);
   if (bs_log2 < 0) return PKV_ERR_UNSUPPORTED;
   if (num_tokens == 0) return PKV_OK;
@@ -499,7 +501,7 @@ pkv_status rope_reshape_and_cache(void* query, const void* key, const void* valu
       max_position <= 0)
     return PKV_ERR_INVALID_ARG;
   if (!valid_dtypes(src_dtype, kv_dtype)) return PKV_ERR_UNSUPPORTED;
-  if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256) return PKV_ERR_UNSUPPORTED;
   const int bs_log2 = block_log2(block_size);
   if (bs_log2 < 0) return PKV_ERR_UNSUPPORTED;
   if (rot_dim < 16 || rot_dim > head_dim || rot_dim % 16 != 0) return PKV_ERR_INVALID_ARG;

@@ -56,11 +56,39 @@ struct PageGeom {
     uint32_t off = r * BOX_ROW_BYTES + x;
     return off ^ (((off >> 7) & SWZ_MASK) << 4);
   }
+  // Byte offset inside a page of byte x of row r, for rows of any width (a
+  // row wider than one box continues in the next box).
+  __device__ __forceinline__ static uint32_t row_off(uint32_t r, uint32_t x) {
+    return (x / BOX_ROW_BYTES) * BOX_BYTES + swz(r, x % BOX_ROW_BYTES);
+  }
   // Byte offset inside a page of element (token r, dim d) (16-bit caches).
   __device__ __forceinline__ static uint32_t elem_off(uint32_t r, uint32_t d) {
     return (d / BOX_ELEMS) * BOX_BYTES + swz(r, (d % BOX_ELEMS) * ELT);
   }
 };
+
+// A thread's run of D/8 bytes of row r of an E4M3 page, starting at byte xo
+// (a multiple of D/8), as D/32 words.
+template <int D>
+__device__ __forceinline__ void lds_run(uint32_t (&w)[D / 32], uint32_t page, int r,
+                                        uint32_t xo) {
+  using Geo = PageGeom<D, KV_E4M3>;
+  constexpr int CH = D / 8;
+  if constexpr (CH == 8) {
+    const uint2 v = lds64(page + Geo::row_off(r, xo));
+    w[0] = v.x;
+    w[1] = v.y;
+  } else {
+#pragma unroll
+    for (int j = 0; j < CH / 16; ++j) {
+      const uint4 v = lds128(page + Geo::row_off(r, xo + 16 * j));
+      w[4 * j] = v.x;
+      w[4 * j + 1] = v.y;
+      w[4 * j + 2] = v.z;
+      w[4 * j + 3] = v.w;
+    }
+  }
+}
 
 // Token (0..15) of S accumulator element e (0, 1) of n-tile j for a thread
 // with c = lane % 4.
@@ -133,7 +161,7 @@ __device__ __forceinline__ void qk_page(float (&acc)[NJ][4], int j0,
       const int tok = 8 * j + tn;
 #pragma unroll
       for (int u = 0; u < D / 64; ++u) {
-        uint4 w = lds128(kpage + Geo::swz(tok, 16 * (4 * u + c)));
+        uint4 w = lds128(kpage + Geo::row_off(tok, 16 * (4 * u + c)));
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -180,25 +208,10 @@ __device__ __forceinline__ void pv_page(float (&oacc)[D / 8][4], const uint32_t 
     constexpr int CH = D / 8;                        // bytes per thread per row
     const uint32_t xo = CH * g;
     uint32_t wa[CH / 4], wb[CH / 4], wc[CH / 4], wd[CH / 4];
-    if constexpr (CH == 16) {
-      uint4 a = lds128(vpage + Geo::swz(t0, xo));
-      uint4 b = lds128(vpage + Geo::swz(t1, xo));
-      uint4 cc = lds128(vpage + Geo::swz(8 + t0, xo));
-      uint4 d = lds128(vpage + Geo::swz(8 + t1, xo));
-      wa[0] = a.x; wa[1] = a.y; wa[2] = a.z; wa[3] = a.w;
-      wb[0] = b.x; wb[1] = b.y; wb[2] = b.z; wb[3] = b.w;
-      wc[0] = cc.x; wc[1] = cc.y; wc[2] = cc.z; wc[3] = cc.w;
-      wd[0] = d.x; wd[1] = d.y; wd[2] = d.z; wd[3] = d.w;
-    } else {
-      uint2 a = lds64(vpage + Geo::swz(t0, xo));
-      uint2 b = lds64(vpage + Geo::swz(t1, xo));
-      uint2 cc = lds64(vpage + Geo::swz(8 + t0, xo));
-      uint2 d = lds64(vpage + Geo::swz(8 + t1, xo));
-      wa[0] = a.x; wa[1] = a.y;
-      wb[0] = b.x; wb[1] = b.y;
-      wc[0] = cc.x; wc[1] = cc.y;
-      wd[0] = d.x; wd[1] = d.y;
-    }
+    lds_run<D>(wa, vpage, t0, xo);
+    lds_run<D>(wb, vpage, t1, xo);
+    lds_run<D>(wc, vpage, 8 + t0, xo);
+    lds_run<D>(wd, vpage, 8 + t1, xo);
     if (valid < kBS) {
 #pragma unroll
       for (int i = 0; i < CH / 4; ++i) {

@@ -102,8 +102,8 @@ __device__ __forceinline__ void load_e4m3_page(E4M3PageRegs<D>& r, uint32_t kpag
   const int t0 = g ^ ((g & 1) << 2);
 #pragma unroll
   for (int u = 0; u < D / 64; ++u) {
-    r.k[0][u] = lds128(kpage + Geo::swz(t0, 16 * (4 * u + c)));
-    r.k[1][u] = lds128(kpage + Geo::swz(8 + t0, 16 * (4 * u + c)));
+    r.k[0][u] = lds128(kpage + Geo::row_off(t0, 16 * (4 * u + c)));
+    r.k[1][u] = lds128(kpage + Geo::row_off(8 + t0, 16 * (4 * u + c)));
   }
   const int ta = 2 * c, tb = (2 * c + 1) ^ 4;
   constexpr int CH = D / 8;
@@ -111,13 +111,7 @@ __device__ __forceinline__ void load_e4m3_page(E4M3PageRegs<D>& r, uint32_t kpag
   const int rows[4] = {ta, tb, 8 + ta, 8 + tb};
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    if constexpr (CH == 16) {
-      const uint4 w = lds128(vpage + Geo::swz(rows[q], xo));
-      r.v[q][0] = w.x; r.v[q][1] = w.y; r.v[q][2] = w.z; r.v[q][3] = w.w;
-    } else {
-      const uint2 w = lds64(vpage + Geo::swz(rows[q], xo));
-      r.v[q][0] = w.x; r.v[q][1] = w.y;
-    }
+    lds_run<D>(r.v[q], vpage, rows[q], xo);
   }
 }
 
@@ -190,8 +184,8 @@ __device__ __forceinline__ void kq_page(float (&acc)[NT][4], const uint32_t (&qf
     uint4 raw[2][D / 64];
 #pragma unroll
     for (int u = 0; u < D / 64; ++u) {
-      raw[0][u] = lds128(kpage + Geo::swz(t0, 16 * (4 * u + c)));
-      raw[1][u] = lds128(kpage + Geo::swz(8 + t0, 16 * (4 * u + c)));
+      raw[0][u] = lds128(kpage + Geo::row_off(t0, 16 * (4 * u + c)));
+      raw[1][u] = lds128(kpage + Geo::row_off(8 + t0, 16 * (4 * u + c)));
     }
     kq_regs<D, NT>(acc, qf, raw);
   } else {
@@ -241,25 +235,10 @@ __device__ __forceinline__ void vp_page(float (&oacc)[NT][D / 16][4], const uint
     constexpr int CH = D / 8;                      // bytes per token row for this thread
     const uint32_t xo = CH * g;
     uint32_t wa[CH / 4], wb[CH / 4], wc[CH / 4], wd[CH / 4];
-    if constexpr (CH == 16) {
-      const uint4 a = lds128(vpage + Geo::swz(ta, xo));
-      const uint4 b = lds128(vpage + Geo::swz(tb, xo));
-      const uint4 cc = lds128(vpage + Geo::swz(8 + ta, xo));
-      const uint4 d = lds128(vpage + Geo::swz(8 + tb, xo));
-      wa[0] = a.x; wa[1] = a.y; wa[2] = a.z; wa[3] = a.w;
-      wb[0] = b.x; wb[1] = b.y; wb[2] = b.z; wb[3] = b.w;
-      wc[0] = cc.x; wc[1] = cc.y; wc[2] = cc.z; wc[3] = cc.w;
-      wd[0] = d.x; wd[1] = d.y; wd[2] = d.z; wd[3] = d.w;
-    } else {
-      const uint2 a = lds64(vpage + Geo::swz(ta, xo));
-      const uint2 b = lds64(vpage + Geo::swz(tb, xo));
-      const uint2 cc = lds64(vpage + Geo::swz(8 + ta, xo));
-      const uint2 d = lds64(vpage + Geo::swz(8 + tb, xo));
-      wa[0] = a.x; wa[1] = a.y;
-      wb[0] = b.x; wb[1] = b.y;
-      wc[0] = cc.x; wc[1] = cc.y;
-      wd[0] = d.x; wd[1] = d.y;
-    }
+    lds_run<D>(wa, vpage, ta, xo);
+    lds_run<D>(wb, vpage, tb, xo);
+    lds_run<D>(wc, vpage, 8 + ta, xo);
+    lds_run<D>(wd, vpage, 8 + tb, xo);
 #pragma unroll
     for (int i = 0; i < CH / 4; ++i) {
       // dims (D/8) g + 4i + {0,1} -> m-tile 2i, {2,3} -> m-tile 2i+1

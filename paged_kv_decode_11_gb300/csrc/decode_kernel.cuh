@@ -153,6 +153,10 @@ __global__ void __launch_bounds__(NW * 32)
     if constexpr (GATHER) {
       const int* rows = s_ids + (warp + NW * k) * kBS;
       constexpr int CPR = Geo::ROW_BYTES / 16;             // 16-byte chunks per row
+      // Copies a lane keeps in flight: NST stages of K and V. Configurations
+      // up to 32 ran on GB300; one with 64 (bf16, D = 256, two stages) raised
+      // an illegal-instruction fault, so the gather path stays within 32.
+      static_assert(NST * 2 * kBS * CPR / 32 <= 32, "too many cp.async in flight per thread");
 #pragma unroll
       for (int u = 0; u < kBS * CPR / 32; ++u) {
         const int ch = lane + 32 * u, r = ch / CPR, x = (ch % CPR) * 16;
@@ -381,9 +385,15 @@ __global__ void __launch_bounds__(NW * 32)
         const float w = (ls == -INFINITY || M == -INFINITY) ? 0.f : exp2f(ls - M);
         z[j] += w;
         const float* o = p.ws_o + wrow * D + lane * PER;
-        if constexpr (PER == 4) {
-          const float4 v = __ldcg(reinterpret_cast<const float4*>(o));
-          acc[j][0] += w * v.x; acc[j][1] += w * v.y; acc[j][2] += w * v.z; acc[j][3] += w * v.w;
+        if constexpr (PER % 4 == 0) {
+#pragma unroll
+          for (int v4 = 0; v4 < PER / 4; ++v4) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(o) + v4);
+            acc[j][4 * v4] += w * v.x;
+            acc[j][4 * v4 + 1] += w * v.y;
+            acc[j][4 * v4 + 2] += w * v.z;
+            acc[j][4 * v4 + 3] += w * v.w;
+          }
         } else {
           const float2 v = __ldcg(reinterpret_cast<const float2*>(o));
           acc[j][0] += w * v.x; acc[j][1] += w * v.y;
@@ -470,7 +480,11 @@ static pkv_status launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK,
 template <bool GATHER, int D, int KV, bool QBF16>
 static pkv_status launch_decode_nt(const DecodeParams& p, const CUtensorMap& tmK,
                                    const CUtensorMap& tmV, cudaStream_t stream, bool prog) {
-  if (p.G > 8) return launch_decode_t<GATHER, D, KV, QBF16, 2>(p, tmK, tmV, stream, prog);
+  if constexpr (D <= 128) {
+    if (p.G > 8) return launch_decode_t<GATHER, D, KV, QBF16, 2>(p, tmK, tmV, stream, prog);
+  } else {
+    if (p.G > 8) return PKV_ERR_UNSUPPORTED;        // 16 head columns at D = 256: not built
+  }
   return launch_decode_t<GATHER, D, KV, QBF16, 1>(p, tmK, tmV, stream, prog);
 }
 
@@ -491,6 +505,12 @@ template <bool GATHER>
 pkv_status launch_decode_mode(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                               pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
                               cudaStream_t stream, bool prog) {
+  if constexpr (GATHER) {
+    if (head_dim == 256) return PKV_ERR_UNSUPPORTED;   // rows too wide for the gather path
+  } else {
+    if (head_dim == 256)
+      return launch_decode_d<GATHER, 256>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);
+  }
   if (head_dim == 128)
     return launch_decode_d<GATHER, 128>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);
   return launch_decode_d<GATHER, 64>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);

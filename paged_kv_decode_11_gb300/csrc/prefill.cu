@@ -248,8 +248,9 @@ __global__ void __launch_bounds__((kPrefillConsumers + 1) * 32)
 template <int D, int KV, bool QBF16>
 static pkv_status launch_prefill_t(const PrefillParams& p, const CUtensorMap& tmK,
                                    const CUtensorMap& tmV, cudaStream_t stream) {
-  constexpr int NST = 3;
-  constexpr int KT = 4;
+  // D = 256: two pages per tile and two stages keep registers and shared memory in bounds
+  constexpr int NST = D > 128 ? 2 : 3;
+  constexpr int KT = D > 128 ? 2 : 4;
   using Cfg = PrefillCfg<D, KV, NST, KT>;
   auto kern = prefill_chunk_kernel<D, KV, QBF16, NST, KT>;
   int dev = 0;
@@ -282,6 +283,7 @@ static pkv_status launch_prefill_d(const PrefillParams& p, pkv_dtype q_dtype, pk
 pkv_status launch_prefill(const PrefillParams& p, int head_dim, pkv_dtype q_dtype,
                           pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           cudaStream_t stream) {
+  if (head_dim == 256) return launch_prefill_d<256>(p, q_dtype, kv_dtype, tmK, tmV, stream);
   if (head_dim == 128) return launch_prefill_d<128>(p, q_dtype, kv_dtype, tmK, tmV, stream);
   return launch_prefill_d<64>(p, q_dtype, kv_dtype, tmK, tmV, stream);
 }

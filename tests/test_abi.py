@@ -64,7 +64,9 @@ def _decode(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,want", [
-    (dict(D=96), UNSUPPORTED), (dict(BS=3), UNSUPPORTED), (dict(BS=48), UNSUPPORTED),
+    (dict(D=96), UNSUPPORTED), (dict(D=512), UNSUPPORTED), (dict(D=256, Hq=32, Hkv=2), UNSUPPORTED),
+    (dict(BS=3), UNSUPPORTED), (dict(BS=48), UNSUPPORTED), (dict(D=256, B=0, out=None), OK),
+    (dict(D=256, BS=8), UNSUPPORTED),
     (dict(BS=1, B=0, out=None), OK), (dict(BS=8, B=0, out=None), OK),
     (dict(BS=1, part=4096), UNSUPPORTED), (dict(BS=16, part=4096, B=0, out=None), OK),
     (dict(BS=128), UNSUPPORTED), (dict(BS=32, B=0, out=None), OK),
@@ -114,7 +116,7 @@ def _prefill(lib, **kw):
 
 
 @pytest.mark.parametrize("kw,want", [
-    (dict(D=256), UNSUPPORTED), (dict(cu=None), INVALID), (dict(kv_dtype=FP8), INVALID),
+    (dict(D=320), UNSUPPORTED), (dict(cu=None), INVALID), (dict(kv_dtype=FP8), INVALID),
     (dict(BS=1), UNSUPPORTED), (dict(T=0, out=None), OK), (dict(Hq=7, Hkv=2), INVALID),
 ])
 def test_prefill_argument_checks(lib, kw, want):
