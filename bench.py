@@ -393,8 +393,10 @@ def run_ours(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": ("e4m3 KV dequantised to f16 for m16n8k16 MMA, fp32 accumulate"
-                      if case.kv_fp8 else f"{case.dtype} m16n8k16 MMA, fp32 accumulate"),
+            "dtype": (("e4m3 KV dequantised to f16 for m16n8k16 MMA, fp32 accumulate"
+                       if case.kv_fp8 else f"{case.dtype} m16n8k16 MMA, fp32 accumulate")
+                      + ("; prefill chunk on tcgen05 MMA (TMEM fp32 accumulators)"
+                         if case.prefill is not None and not case.kv_fp8 else "")),
             "data": "synthetic (seeded N(0,1) values, random block placement)",
             "config": {
                 "workload": workload_desc(case),

@@ -100,6 +100,12 @@ pkv_status launch_cache_write(const CacheWriteParams& p, pkv_dtype src_dtype,
 pkv_status launch_rope_cache(const RopeCacheParams& p, pkv_dtype src_dtype, pkv_dtype kv_dtype,
                              cudaStream_t stream);
 
+// Causal chunked prefill on the fifth-generation tensor cores (16-bit caches,
+// head_dim 64 or 128); the other cases take launch_prefill.
+bool prefill_tc_supported(int head_dim, pkv_dtype kv_dtype);
+pkv_status launch_prefill_tc(const PrefillParams& p, int head_dim, pkv_dtype kv_dtype,
+                             const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t stream);
+
 // Rows of q handled by one prefill CTA for a GQA group size G.
 int prefill_q_tile(int G);
 
