@@ -89,6 +89,7 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
 #define PKV_DEVERR_TIMEOUT    0x8u  /* a bounded wait on an async copy gave up */
 #define PKV_DEVERR_QLEN       0x10u /* prefill: chunk longer than its context */
 #define PKV_DEVERR_POSITION   0x20u /* rotary: position outside [0, max_position) */
+#define PKV_DEVERR_COUNTER    0x40u /* decode: workspace counters were not zero */
 
 /*
  * paged_attn_decode_workspace_size
@@ -120,11 +121,16 @@ size_t paged_attn_decode_workspace_size(int num_seqs, int num_q_heads,
  *   k_scales, v_scales: fp32 [Hkv], required for FP8 KV, ignored otherwise.
  *   out_lse: optional fp32 [B, Hq] (NULL to skip).
  *   workspace: 256-byte aligned device buffer of at least
- *   paged_attn_decode_workspace_size() bytes, always required. Its contents
- *   need no initialisation: when contexts may span several partitions the
- *   call enqueues a clear of its counter region (cudaMemsetAsync on
- *   `stream`) before the kernel. Two calls that share a workspace must not
- *   overlap on the GPU.
+ *   paged_attn_decode_workspace_size() bytes, always required. Zero-fill it
+ *   once before its first use: each call sets the per-(sequence, KV head)
+ *   partition counters it used back to zero (CUDA-graph replays included),
+ *   so a call enqueues nothing but its kernel. A call that ends with a
+ *   device error may leave counters set; zero the workspace again before
+ *   reusing it (PKV_DEVERR_COUNTER reports counters found non-zero). Two
+ *   calls that share a workspace must not overlap on the GPU.
+ *   The kernel is launched as a programmatic dependent of the kernel ahead
+ *   of it on `stream`: it may become resident while that kernel runs, and
+ *   reads no input before that kernel has finished.
  */
 pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype,
                              const void* k_cache, const void* v_cache,

@@ -20,7 +20,7 @@ PKV_F16, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
           3: "workspace missing or too small", 4: "CUDA error", 5: "device-side check failed"}
 DEVERR_BITS = {0x1: "block id", 0x2: "slot", 0x4: "seq_len", 0x8: "timeout", 0x10: "chunk length",
-               0x20: "rotary position"}
+               0x20: "rotary position", 0x40: "workspace counters not zero"}
 
 # Every symbol include/pkv.h declares.
 EXPORTS = ("paged_attn_decode_workspace_size", "paged_attn_decode", "paged_attn_decode_noalloc",
@@ -123,15 +123,15 @@ def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
                       out_lse: Optional[torch.Tensor] = None,
                       workspace: Optional[torch.Tensor] = None, stream=None) -> None:
     """out[B, Hq, D] <- decode attention of q[B, Hq, D] over the paged cache
-    k_cache/v_cache[num_blocks, Hkv, 16, D]. A workspace tensor is allocated
-    with torch when none is given."""
+    k_cache/v_cache[num_blocks, Hkv, BS, D]. A zero-filled workspace tensor
+    is allocated with torch when none is given (reuse one across calls)."""
     B, Hq, D = q.shape
     nb, hkv, bs, d2 = k_cache.shape
     assert d2 == D and out.shape == q.shape and out.dtype == q.dtype
     assert block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32
     if workspace is None:
         ws = paged_attn_decode_workspace_size(B, Hq, hkv, D, max_seq_len, partition_tokens)
-        workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=q.device)
     st = load().paged_attn_decode(
         _dev_ptr(out, "out"), _dev_ptr(q, "q"), dtype_code(q), _dev_ptr(k_cache, "k_cache"),
         _dev_ptr(v_cache, "v_cache"), dtype_code(k_cache), _dev_ptr(block_tables, "block_tables"),
@@ -206,7 +206,7 @@ def paged_attn_varlen(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
     if workspace is None:
         ws = paged_attn_decode_workspace_size(num_decode_seqs, Hq, hkv, D, max_decode_seq_len,
                                               partition_tokens)
-        workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=q.device)
+        workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=q.device)
     st = load().paged_attn_varlen(
         _dev_ptr(out, "out"), _dev_ptr(q, "q"), dtype_code(q), _dev_ptr(k_cache, "k_cache"),
         _dev_ptr(v_cache, "v_cache"), dtype_code(k_cache), _dev_ptr(block_tables, "block_tables"),

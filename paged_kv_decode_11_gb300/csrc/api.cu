@@ -183,15 +183,12 @@ size_t paged_attn_decode_workspace_size(int num_seqs, int num_q_heads, int num_k
 
 namespace {
 
-// A decode call checked and planned, ready to enqueue: the counter reset
-// (memset_bytes at p.done, 0 when a sequence has one partition at most) and
-// the kernel launch.
+// A decode call checked and planned, ready to enqueue (one kernel launch).
 struct DecodeCall {
   DecodeParams p;
   CUtensorMap tmK, tmV;
   int head_dim;
   pkv_dtype q_dtype, kv_dtype;
-  size_t memset_bytes;
   bool empty;
 };
 
@@ -246,8 +243,6 @@ pkv_status decode_setup(void* out, const void* q, pkv_dtype q_dtype, const void*
   unsigned int* err = err_word();
   if (err == nullptr) return PKV_ERR_CUDA;
   char* ws = static_cast<char*>(workspace);
-  // the partition counters start from zero in every call
-  call->memset_bytes = pl.max_parts > 1 ? pl.off_o : 0;
   call->head_dim = head_dim;
   call->q_dtype = q_dtype;
   call->kv_dtype = kv_dtype;
@@ -278,19 +273,20 @@ pkv_status decode_setup(void* out, const void* q, pkv_dtype q_dtype, const void*
   p.part = pl.part;
   p.max_parts = pl.max_parts;
   p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+  p.wait_prior = 1;
   return PKV_OK;
 }
 
-pkv_status decode_reset(const DecodeCall& c, cudaStream_t stream) {
-  if (c.empty || c.memset_bytes == 0) return PKV_OK;
-  return cudaMemsetAsync(c.p.done, 0, c.memset_bytes, stream) == cudaSuccess ? PKV_OK
-                                                                            : PKV_ERR_CUDA;
-}
-
-pkv_status decode_launch(const DecodeCall& c, cudaStream_t stream, bool programmatic) {
+// Decode is always launched as a programmatic dependent of the kernel ahead
+// of it on the stream. With wait_prior it waits for that kernel before
+// reading anything (behind a cache write: its launch overlaps the write);
+// without, it runs beside it (behind the prefill of the same step, whose
+// inputs it does not touch).
+pkv_status decode_launch(const DecodeCall& c, cudaStream_t stream, bool beside_prior) {
   if (c.empty) return PKV_OK;
-  return launch_decode(c.p, c.head_dim, c.q_dtype, c.kv_dtype, c.tmK, c.tmV, stream,
-                       programmatic);
+  DecodeParams p = c.p;
+  p.wait_prior = beside_prior ? 0 : 1;
+  return launch_decode(p, c.head_dim, c.q_dtype, c.kv_dtype, c.tmK, c.tmV, stream, true);
 }
 
 
@@ -390,7 +386,6 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const 
                                workspace_bytes, &c);
   if (st != PKV_OK || c.empty) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if ((st = decode_reset(c, s)) != PKV_OK) return st;
   return decode_launch(c, s, false);
 }
 
@@ -449,10 +444,9 @@ pkv_status paged_attn_varlen(void* out, const void* q, pkv_dtype q_dtype, const 
                      v_scales, out_lse, &pc);
   if (st != PKV_OK) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // counter reset, then the prefill chunks, then decode: decode is launched
-  // as a programmatic dependent of the prefill kernel, whose CTAs release it
-  // as they start, so both kinds of work share the GPU without a second stream
-  if ((st = decode_reset(dc, s)) != PKV_OK) return st;
+  // the prefill chunks, then decode launched as a programmatic dependent of
+  // the prefill kernel, whose CTAs release it as they start, so both kinds of
+  // work share the GPU without a second stream
   if ((st = prefill_launch(pc, s)) != PKV_OK) return st;
   return decode_launch(dc, s, !pc.empty);
 }

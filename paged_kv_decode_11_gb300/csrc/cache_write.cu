@@ -21,6 +21,9 @@ namespace pkv {
 
 template <bool SRC_BF16, bool TO_FP8>
 __global__ void __launch_bounds__(256) cache_write_kernel(const CacheWriteParams p) {
+  // a decode launched behind this kernel may become resident now; it waits
+  // for this grid to finish before it reads anything
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const int chunks = p.D / 8;
   const int64_t total = (int64_t)p.num_tokens * p.Hkv * chunks;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;

@@ -77,6 +77,9 @@ __global__ void __launch_bounds__(NW * 32)
   const int g = lane >> 2, c = lane & 3;
   const int part_idx = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int G = p.G;
+  // launched as a programmatic dependent: the CTA is resident early, and
+  // reads nothing before the kernel ahead of it (the cache write) is done
+  if (p.wait_prior) griddep_wait();
 
   int ctx = p.seq_lens[b];
   const int cap = min(p.max_seq_len, p.max_blocks << p.bs_log2);
@@ -344,13 +347,20 @@ __global__ void __launch_bounds__(NW * 32)
   // ---- the CTA that completes the last partition of (b, h) merges them ------------------
   __threadfence();
   __syncthreads();
+  // Finished-partition counter of (b, h). The CTA that completes the count
+  // merges and sets it back to zero, so the workspace is ready for the next
+  // call (a CUDA-graph replay included) without a clear of its own. A count
+  // at or past nparts means the counters did not start at zero.
+  unsigned long long* ctr = p.done + (int64_t)b * p.Hkv + h;
   if (tid == 0) {
-    const unsigned long long before = atomicAdd(p.done + (int64_t)b * p.Hkv + h, 1ull);
+    const unsigned long long before = atomicAdd(ctr, 1ull);
+    if (before >= (unsigned long long)nparts) atomicOr(p.err, PKV_DEVERR_COUNTER);
     s_last = (before + 1 == (unsigned long long)nparts);
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  if (tid == 0) *ctr = 0ull;
   // The warps split the partitions; each lane owns D/32 dims of every head.
   // Pass 1: the largest log2-sum-exp of each head.
   constexpr int PER = D / 32;

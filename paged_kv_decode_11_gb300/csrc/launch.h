@@ -24,7 +24,7 @@ struct DecodeParams {
   const float* k_scales;
   const float* v_scales;
   float* out_lse;
-  unsigned long long* done;   // [B * Hkv] finished-partition counters (zero at launch)
+  unsigned long long* done;   // [B * Hkv] finished-partition counters (zero between calls)
   float* ws_o;                // [B * Hq, max_parts, D] fp32 partition outputs (normalised)
   float* ws_lse;              // [B * Hq, max_parts]    fp32 partition log2-sum-exp
   unsigned int* err;          // device error word
@@ -33,6 +33,7 @@ struct DecodeParams {
   int bs_log2;                // log2(block_size)
   int part, max_parts;        // partition size (tokens) and partitions per sequence
   float qk_scale_log2;        // scale * log2(e)
+  int wait_prior;             // wait for the grids ahead of it on the stream before reading
 };
 
 struct PrefillParams {

@@ -185,6 +185,9 @@ __device__ __forceinline__ Pair8 rotate_item(const uint16_t* row, const float* c
 
 template <bool BF16, bool TO_FP8, bool NEOX>
 __global__ void __launch_bounds__(256) rope_cache_kernel(const RopeCacheParams p) {
+  // a decode launched behind this kernel may become resident now; it waits
+  // for this grid to finish before it reads anything
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const int R = p.rot / 16;                 // rotation items per head
   const int PT = (p.D - p.rot) / 8;         // pass-through chunks per key head
   const int C8 = p.D / 8;                   // chunks per value head

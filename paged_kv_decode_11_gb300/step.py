@@ -44,7 +44,7 @@ class DecodeStep:
         Bn, Hq, D = q.shape
         ws = B.paged_attn_decode_workspace_size(Bn, Hq, k_cache.shape[1], D, self.max_seq_len,
                                                 self.partition_tokens)
-        self.workspace = torch.empty(max(ws, 256), dtype=torch.uint8, device=q.device)
+        self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=q.device)
 
     @classmethod
     def from_case(cls, case, k_cache, v_cache):

@@ -205,6 +205,45 @@ def test_decode_rejects_missing_workspace():
 
 # ---- full-size workloads, sampled outputs ----------------------------------------
 
+def test_decode_workspace_counters_reset_themselves():
+    """Many calls on one zero-filled workspace, with sequences split into many
+    partitions: every call merges the same way (the counters come back to
+    zero each time) and no device error is raised."""
+    c = make_case("tiny", 8, kv="fp8", ctx=("fixed", [700, 33, 520, 1]), pool=("blocks", 128))
+    kc, vc = product_cache(c)
+    ks, vs = scales(c)
+    q = dev(c.q)
+    bt, sl = dev(c.block_tables), dev(c.seq_lens)
+    ws = torch.zeros(P.paged_attn_decode_workspace_size(c.B, c.Hq, c.Hkv, c.D, c.max_seq_len, 32),
+                     dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(6):
+        out = torch.empty_like(q)
+        P.paged_attn_decode(out, q, kc, vc, bt, sl, float(c.scale), c.max_seq_len, ks, vs,
+                            partition_tokens=32, workspace=ws)
+        outs.append(out)
+    torch.cuda.synchronize()
+    check_device_ok()
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
+    assert int(ws[:c.B * c.Hkv * 8].view(torch.int64).abs().sum()) == 0
+    ko, vo = oracle_cache(c)
+    want, _ = oracle_decode(c, ko, vo)
+    assert_close(outs[-1], want, tol(c), "after repeated calls")
+
+
+def test_decode_reports_counters_left_nonzero():
+    c = make_case("tiny", 9, ctx=("fixed", [700, 33, 520, 1]), pool=("blocks", 128))
+    kc, vc = product_cache(c)
+    q = dev(c.q)
+    ws = torch.zeros(P.paged_attn_decode_workspace_size(c.B, c.Hq, c.Hkv, c.D, c.max_seq_len, 32),
+                     dtype=torch.uint8, device="cuda")
+    ws[:8].view(torch.int64)[0] = 1000           # a counter a failed call could have left
+    out = torch.empty_like(q)
+    P.paged_attn_decode(out, q, kc, vc, dev(c.block_tables), dev(c.seq_lens), float(c.scale),
+                        c.max_seq_len, partition_tokens=32, workspace=ws)
+    assert P.pkv_get_device_error() & 0x40
+
+
 @pytest.mark.parametrize("name,sel", [("qwen2.5-7b", [0, 5, 17, 31]),
                                       ("llama3-8b-fp8", [0, 9, 64, 127]),
                                       ("long-ctx", [0, 3])])
