@@ -125,10 +125,11 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Split-KV plan of a decode call: contexts are cut into partitions of
 // `part` tokens (one CTA each). The automatic size is the smallest power of
-// two from 256 to 2048 tokens that keeps the launch at about 3 waves of
+// two from 512 to 2048 tokens that keeps the launch at about 3 waves of
 // resident CTAs when contexts average half the maximum (fewer, larger
 // partitions cost less per CTA and leave fewer partials to merge; enough of
-// them keep every SM busy).
+// them keep every SM busy). Below 512 tokens the per-CTA start and merge
+// cost more than the extra parallelism gives back.
 // Workspace: [done counters B*Hkv u64 | partition outputs B*Hq*max_parts*D
 // fp32 | partition log2-sum-exps B*Hq*max_parts fp32], each region 256-byte
 // aligned.
@@ -145,7 +146,7 @@ DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head
   } else {
     const int64_t est = (int64_t)num_seqs * num_kv_heads * std::max(1, max_seq_len / 2);
     const int64_t target = (int64_t)(sms > 0 ? sms : 148) * kDecodeWorkers * 3;
-    pl.part = 256;
+    pl.part = 512;
     while (pl.part < 2048 && est / pl.part > target) pl.part *= 2;
   }
   pl.max_parts = std::max(1, (max_seq_len + pl.part - 1) / pl.part);
