@@ -163,9 +163,10 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype,
  *   rejected with PKV_ERR_WORKSPACE before anything is launched.
  *   Nothing here allocates. The first call on a device looks up the array's
  *   device address (cudaGetSymbolAddress); make that first call before any
- *   stream capture. Every call on a device shares the one array and each
- *   call clears the counters it needs, so calls that overlap on the GPU (on
- *   different streams, or from different threads) race: serialise them.
+ *   stream capture. The array starts zero-filled and each call leaves the
+ *   counters it used at zero. Every call on a device shares the one array,
+ *   so calls that overlap on the GPU (on different streams, or from
+ *   different threads) race: serialise them.
  */
 pkv_status paged_attn_decode_noalloc(void* out, const void* q, pkv_dtype q_dtype,
                                      const void* k_cache, const void* v_cache,

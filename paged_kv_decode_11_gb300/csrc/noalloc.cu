@@ -59,8 +59,8 @@ extern "C" pkv_status paged_attn_decode_noalloc(
     scratch = scratch_address();
     if (scratch == nullptr) return PKV_ERR_CUDA;
   }
-  // The shared scratch is the workspace; the decode call clears the counters
-  // it needs before its kernel runs.
+  // The shared scratch is the workspace. It starts zero-filled (a device
+  // global) and every call leaves its counters at zero again.
   return paged_attn_decode(out, q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, seq_lens,
                            num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                            max_blocks_per_seq, num_blocks, max_seq_len, scale, k_scales, v_scales,
