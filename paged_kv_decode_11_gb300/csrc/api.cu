@@ -360,10 +360,12 @@ pkv_status prefill_setup(void* out, const void* q, pkv_dtype q_dtype, const void
   return PKV_OK;
 }
 
-pkv_status prefill_launch(const PrefillCall& c, cudaStream_t stream) {
+// beside_decode: a decode grid is launched right behind this one to run on
+// the SMs it leaves free
+pkv_status prefill_launch(const PrefillCall& c, cudaStream_t stream, bool beside_decode) {
   if (c.empty) return PKV_OK;
   if (prefill_tc_supported(c.head_dim, c.kv_dtype))
-    return launch_prefill_tc(c.p, c.head_dim, c.kv_dtype, c.tmK, c.tmV, stream);
+    return launch_prefill_tc(c.p, c.head_dim, c.kv_dtype, c.tmK, c.tmV, stream, !beside_decode);
   return launch_prefill(c.p, c.head_dim, c.q_dtype, c.kv_dtype, c.tmK, c.tmV, stream);
 }
 
@@ -405,7 +407,7 @@ pkv_status paged_attn_prefill_chunk(void* out, const void* q, pkv_dtype q_dtype,
                                 max_blocks_per_seq, num_blocks, scale, k_scales, v_scales,
                                 out_lse, &c);
   if (st != PKV_OK || c.empty) return st;
-  return prefill_launch(c, reinterpret_cast<cudaStream_t>(stream));
+  return prefill_launch(c, reinterpret_cast<cudaStream_t>(stream), false);
 }
 
 pkv_status paged_attn_varlen(void* out, const void* q, pkv_dtype q_dtype, const void* k_cache,
@@ -448,7 +450,7 @@ pkv_status paged_attn_varlen(void* out, const void* q, pkv_dtype q_dtype, const 
   // the prefill chunks, then decode launched as a programmatic dependent of
   // the prefill kernel, whose CTAs release it as they start, so both kinds of
   // work share the GPU without a second stream
-  if ((st = prefill_launch(pc, s)) != PKV_OK) return st;
+  if ((st = prefill_launch(pc, s, !dc.empty)) != PKV_OK) return st;
   return decode_launch(dc, s, !pc.empty);
 }
 

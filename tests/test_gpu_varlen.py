@@ -1,7 +1,9 @@
 """paged_attn_varlen: one call over a whole continuous-batching step (decode
 sequences first, then prefill chunks) against the oracle, against the two
-separate entry points (bit for bit: the same kernels compute every row), and
-under CUDA-graph capture."""
+separate entry points (decode rows bit for bit: the same kernel computes
+them; chunk rows within tolerance: alone, a small chunk's keys may be split
+over a cluster of two CTAs, which sums in another order), and under
+CUDA-graph capture."""
 import numpy as np
 import pytest
 import torch
@@ -43,7 +45,8 @@ def test_mixed_step_varlen_vs_oracle_and_two_streams(kv):
     torch.cuda.synchronize()
     check_device_ok()
     assert torch.equal(_bits(one.out), _bits(two.out)), "decode rows differ between modes"
-    assert torch.equal(_bits(one.prefill_out), _bits(two.prefill_out)), "chunk rows differ"
+    assert_close(one.prefill_out, two.prefill_out.double().cpu().numpy(), tol(c),
+                 "chunk rows between modes")
     sel = [0, 7, 16, 40, 63]
     ko, vo = oracle_cache(c)
     want, wlse = oracle_decode(c, ko, vo, sel=sel)
