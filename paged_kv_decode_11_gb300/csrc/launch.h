@@ -91,8 +91,6 @@ pkv_status launch_decode(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
 // Decode for blocks of fewer than 16 tokens (pages gathered row by row).
 pkv_status launch_decode_gather(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                                 pkv_dtype kv_dtype, cudaStream_t stream, bool programmatic);
-// Dynamic shared memory of one decode CTA.
-size_t decode_smem_bytes(int head_dim, pkv_dtype kv_dtype, int G);
 pkv_status launch_prefill(const PrefillParams& p, int head_dim, pkv_dtype q_dtype,
                           pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
                           cudaStream_t stream);
