@@ -165,14 +165,19 @@ class ClockSampler:
 
 # ---- profile-derived traffic ----------------------------------------------------
 
+# The sources the decode kernel and its launch plan are built from: a traffic
+# figure taken by ncu stays valid while none of them changes.
+DECODE_SOURCES = ("api.cu", "common.cuh", "decode.cu", "decode_frags.cuh", "decode_kernel.cuh",
+                  "launch.h", "ptx.cuh")
+
+
 def source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_decode_11_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in DECODE_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
