@@ -345,21 +345,22 @@ __global__ void __launch_bounds__(NW * 32)
   if (nparts == 1) return;
 
   // ---- the CTA that completes the last partition of (b, h) merges them ------------------
-  __threadfence();
-  __syncthreads();
   // Finished-partition counter of (b, h). The CTA that completes the count
   // merges and sets it back to zero, so the workspace is ready for the next
   // call (a CUDA-graph replay included) without a clear of its own. A count
-  // at or past nparts means the counters did not start at zero.
+  // at or past nparts means the counters did not start at zero. One thread
+  // bumps it with release semantics after the barrier (publishing every
+  // thread's partial writes) and acquire semantics (so the merging CTA,
+  // after the next barrier, reads every other partition's writes).
+  __syncthreads();
   unsigned long long* ctr = p.done + (int64_t)b * p.Hkv + h;
   if (tid == 0) {
-    const unsigned long long before = atomicAdd(ctr, 1ull);
+    const unsigned long long before = atom_add_acq_rel_gpu(ctr, 1ull);
     if (before >= (unsigned long long)nparts) atomicOr(p.err, PKV_DEVERR_COUNTER);
     s_last = (before + 1 == (unsigned long long)nparts);
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   if (tid == 0) *ctr = 0ull;
   // The warps split the partitions; each lane owns D/32 dims of every head.
   // Pass 1: the largest log2-sum-exp of each head.

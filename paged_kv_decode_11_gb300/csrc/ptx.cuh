@@ -241,6 +241,21 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 
 __device__ __forceinline__ float ldcg_f32(const float* p) { return __ldcg(p); }
 
+// Atomic add at GPU scope with acquire and release semantics; returns the old
+// value. Issued by one thread right after a CTA barrier, the release makes the
+// whole CTA's earlier writes visible before the add (release is cumulative
+// over what the barrier ordered before it), and the acquire orders the reads
+// that follow the next barrier after every write released by earlier adds.
+__device__ __forceinline__ unsigned long long atom_add_acq_rel_gpu(unsigned long long* p,
+                                                                   unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;"
+               : "=l"(old)
+               : "l"(p), "l"(v)
+               : "memory");
+  return old;
+}
+
 }  // namespace pkv
 
 namespace pkv {
