@@ -9,23 +9,28 @@
 // tensor cores with its accumulators in tensor memory:
 //
 //   CTA = (query tile, KV head, chunk). Tile rows are (query token, head of
-//   the GQA group) pairs, 128 of them: the MMA M. Warp 4 streams K and V
-//   tiles of 4 pages (64 keys) through a TMA ring. Warp 5 issues
+//   the GQA group) pairs, 128 of them: the MMA M. Warp 8 streams K and V
+//   tiles of 4 pages (64 keys) through a TMA ring. Warp 9 issues
 //     S[128 x 64]  = Q[128 x D] . K_tile^T   (K-major A and B, fp32 in TMEM)
 //   and, once the softmax has written P,
-//     O[128 x D]  += P[128 x 64] . V_tile     (V read MN-major)
-//   Warps 0-3 own 32 TMEM lanes each: thread r holds row r of S, so the row
-//   max and sum need no shuffles. O and the row sum are kept relative to a
-//   reference max that moves only when the row max grows by more than 2^8,
-//   so O in TMEM is rescaled rarely; the result is the same softmax.
+//     O_g[128 x D] += P[128 x 64] . V_tile   (V read MN-major)
+//   Two softmax groups of four warps take the key tiles in turn (group g the
+//   tiles u with u % 2 == g), each with its own S buffers, P buffers and O
+//   accumulator, so one group's softmax runs while the other waits on the
+//   tensor cores. In a group, warp w owns TMEM lanes 32 (w % 4) ..: thread r
+//   holds row r of S, so the row max and sum need no shuffles. O_g and the
+//   row sum are kept relative to a reference max that moves only when the
+//   row max grows by more than 2^8, so O in TMEM is rescaled rarely. At the
+//   end the two groups' (O, max, sum) are merged by log-sum-exp, the same
+//   softmax.
 //
 // Shared memory: Q [D/64][128 rows][128 B], then NST stages of
-// K [D/64][4 pages][16 rows][128 B] and V (same), then two P buffers
-// [128 rows][128 B] (S has two TMEM buffers likewise, so the S product of
-// the next tile runs while this one's softmax does),
-// all in the 128-byte swizzled layout (tc.cuh). Placing the four pages of a
-// 64-byte column block back to back gives every operand a uniform 1 KB
-// stride between 8-row groups.
+// K [D/64][4 pages][16 rows][128 B] and V (same), then four P buffers
+// [128 rows][128 B] (two per group; S has two TMEM buffers per group
+// likewise, so the S product of a group's next tile runs while its softmax
+// does), all in the 128-byte swizzled layout (tc.cuh). Placing the four
+// pages of a 64-byte column block back to back gives every operand a
+// uniform 1 KB stride between 8-row groups.
 #include <cuda.h>
 #include "common.cuh"
 #include "launch.h"
@@ -34,6 +39,7 @@
 namespace pkv {
 
 constexpr int kTcRows = 128;                  // query rows per CTA (MMA M)
+constexpr int kTcThreads = 320;               // 2 softmax groups of 4 warps, TMA warp, MMA warp
 constexpr int kTcKeys = 64;                   // keys per tile (S MMA N)
 constexpr int kTcPages = kTcKeys / kBS;
 constexpr float kRescaleLog2 = 8.f;           // reference-max slack (log2 units)
@@ -46,9 +52,10 @@ struct PrefillTcCfg {
   static constexpr int KV_BOX = kTcPages * kBS * 128;        // one column block of a K/V tile
   static constexpr int KV_BYTES = NBOX * KV_BOX;
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;
-  static constexpr int P_BYTES = kTcRows * 128;              // one P buffer (two are kept)
-  static constexpr int SMEM_BYTES = 1024 + Q_BYTES + NST * STAGE_BYTES + 2 * P_BYTES;
-  static constexpr uint32_t TMEM_COLS = 256;                  // S0, S1, O
+  static constexpr int P_BYTES = kTcRows * 128;              // one P buffer (2 per group)
+  static constexpr int SMEM_BYTES = 1024 + Q_BYTES + NST * STAGE_BYTES + 4 * P_BYTES;
+  static constexpr uint32_t TMEM_COLS = 512;                  // 4 S buffers, 2 O
+  static_assert(4 * kTcKeys + 2 * D <= (int)TMEM_COLS, "tensor memory");
 };
 
 __device__ __forceinline__ uint32_t swz128(uint32_t r, uint32_t chunk) {
@@ -81,9 +88,13 @@ __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-               ::: "memory");
+// Split cluster barrier: every thread arrives once after the CTA's barriers
+// are initialised and waits once before its first access to another CTA.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
@@ -115,15 +126,24 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
   return false;
 }
 
+// n consecutive fp32 TMEM columns (n = 16 or 32) of this thread's lane.
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[N]) {
+  static_assert(N == 16 || N == 32, "16 or 32 columns");
+  if constexpr (N == 32) tc::ld32(taddr, v);
+  else tc::ld16(taddr, v);
+}
+
 template <int D, bool BF16, int NST, int SPLIT>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
   using Cfg = PrefillTcCfg<D, NST>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full_bar[NST];
   __shared__ uint64_t empty_bar[NST];
-  __shared__ uint64_t s_bar[2], o_bar[2], p_bar[2];
+  // per softmax group g and buffer b: S ready, P written, P.V done
+  __shared__ uint64_t s_bar[2][2], o_bar[2][2], p_bar[2][2];
   __shared__ uint64_t ready_bar, recv_bar;              // cluster hand-off (SPLIT == 2)
   __shared__ uint32_t tmem_base;
 
@@ -132,7 +152,7 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) griddep_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int qt = blockIdx.x / SPLIT, h = blockIdx.y, n = blockIdx.z;
-  const int split = SPLIT > 1 ? (int)cluster_rank() : 0;  // the leader is split 0
+  const int split = SPLIT > 1 ? (int)cluster_rank() : 0;
   const int G = p.G;
   const int q0 = p.cu_q_lens[n];
   const int L = p.cu_q_lens[n + 1] - q0;
@@ -148,7 +168,8 @@ __global__ void __launch_bounds__(192, 1)
   const int key_end = P0 + i1;                          // keys any row of the tile sees: < key_end
   const int n_pages = (key_end + kBS - 1) / kBS;
   const int n_tiles_all = (key_end + kTcKeys - 1) / kTcKeys;
-  // this CTA's share of the key tiles: [t_begin, t_begin + n_tiles)
+  // this CTA's share of the key tiles: [t_begin, t_begin + n_tiles); its
+  // local tile u goes to softmax group u % 2
   const int per_split = (n_tiles_all + SPLIT - 1) / SPLIT;
   const int t_begin = split * per_split;
   const int n_tiles = max(0, min(n_tiles_all, t_begin + per_split) - t_begin);
@@ -159,36 +180,94 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* basep = smem_raw + (base - raw);
   const uint32_t sQ = base;
   const uint32_t sKV = base + Cfg::Q_BYTES;
-  const uint32_t sP = sKV + NST * Cfg::STAGE_BYTES;
+  const uint32_t sP = sKV + NST * Cfg::STAGE_BYTES;    // [group][buffer] P tiles
   uint8_t* pQ = basep;
   uint8_t* pKV = basep + Cfg::Q_BYTES;
   uint8_t* pP = pKV + NST * Cfg::STAGE_BYTES;
 
-  if (tid == 0) {
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+  bool failed = false;                                  // a wait ran out: stop waiting
+  auto wait = [&](uint64_t* bar, uint32_t parity) {
+    if (failed) return;
+    if (!mbar_wait_bounded(bar, parity)) {
+      failed = true;
+      atomicOr(p.err, PKV_DEVERR_TIMEOUT);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_bar[s], 1);
-      mbar_init(&o_bar[s], 1);
-      mbar_init(&p_bar[s], kTcRows);                    // every softmax thread
+  };
+
+  // ---- producer (warp 8): K and V tiles through the TMA ring. Its lanes look
+  // up the page rows 32 pages (8 tiles) at a time, one chunk ahead, so no
+  // block-table read waits in front of a TMA issue; lane 0 issues the loads.
+  const int pg_begin = t_begin * kTcPages;
+  const int pg_end = min(n_pages, (t_begin + n_tiles) * kTcPages);
+  auto page_row = [&](int lp) -> int {
+    if (lp >= pg_end) return 0;
+    int id = p.block_tables[(int64_t)n * p.max_blocks + (lp >> p.ppb_shift)];
+    if (id < 0 || id >= p.num_blocks) {
+      atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
+      id = 0;
     }
-    mbar_init(&ready_bar, 1);
-    mbar_init(&recv_bar, kTcRows);
-    fence_barrier_init();
+    return ((id * p.Hkv + h) << p.ppb_shift) + (lp & ((1 << p.ppb_shift) - 1));
+  };
+  static_assert(32 % kTcPages == 0, "a tile's pages lie in one chunk");
+  int z_cur = 0, z_next = 0, chunk = 0;
+  auto issue = [&](int u) {
+    const int t = t_begin + u, st = u % NST;
+    if ((u * kTcPages) / 32 != chunk) {
+      z_cur = z_next;
+      ++chunk;
+      z_next = page_row(pg_begin + 32 * (chunk + 1) + lane);
+    }
+    const int pg0 = t * kTcPages;
+    const int npg = min(kTcPages, n_pages - pg0);
+    if (lane == 0) mbar_arrive_expect_tx(&full_bar[st], npg * 2 * kBS * D * 2);
+    uint8_t* dst = pKV + st * Cfg::STAGE_BYTES;
+    for (int pg = 0; pg < npg; ++pg) {
+      const int z = __shfl_sync(0xffffffffu, z_cur, (u * kTcPages + pg) % 32);
+      if (lane == 0) {
+#pragma unroll
+        for (int bx = 0; bx < Cfg::NBOX; ++bx) {
+          uint8_t* kd = dst + bx * Cfg::KV_BOX + pg * (kBS * 128);
+          tma_load_3d(kd, &tmK, &full_bar[st], bx * 64, 0, z);
+          tma_load_3d(kd + Cfg::KV_BYTES, &tmV, &full_bar[st], bx * 64, 0, z);
+        }
+      }
+    }
+  };
+  if (warp == 8) {
+    // the producer sets up the barriers and starts the first tiles right away,
+    // while the other warps load the query tile and allocate tensor memory
+    if (lane == 0) {
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      for (int s = 0; s < NST; ++s) {
+        mbar_init(&full_bar[s], 1);
+        mbar_init(&empty_bar[s], 1);
+      }
+      for (int g = 0; g < 2; ++g)
+        for (int b = 0; b < 2; ++b) {
+          mbar_init(&s_bar[g][b], 1);
+          mbar_init(&o_bar[g][b], 1);
+          mbar_init(&p_bar[g][b], kTcRows);             // every thread of the group
+        }
+      mbar_init(&ready_bar, 1);
+      mbar_init(&recv_bar, 2 * kTcRows);
+      fence_barrier_init();
+    }
+    __syncwarp();
+    z_cur = page_row(pg_begin + lane);
+    z_next = page_row(pg_begin + 32 + lane);
+    for (int u = 0; u < NST && u < n_tiles; ++u) issue(u);
   }
   if (warp == 0) tc::alloc(&tmem_base, Cfg::TMEM_COLS);
 
-  // ---- query tile into shared memory; rows past the chunk are zero ------------
+  // ---- query tile into shared memory (warps 4-7); rows past the chunk are zero ----
+  const int grp = warp >> 2;                            // softmax group (warps 0-7)
+  const int r = tid & (kTcRows - 1);                    // this thread's tile row
   const int rows_used = p.q_tile * G;
-  const int r = tid;                                    // this thread's tile row (tid < 128)
-  const bool rvalid = tid < kTcRows && r < rows_used && i0 + r / G < i1;
   const int qi = i0 + r / G;                            // query token within the chunk
   const int hq = h * G + r % G;                         // query head
-  if (tid < kTcRows) {
+  const bool rvalid = r < rows_used && qi < i1;
+  if (grp == 1) {
     const uint16_t* src =
         static_cast<const uint16_t*>(p.q) + ((int64_t)(q0 + (rvalid ? qi : 0)) * p.Hq +
                                              (rvalid ? hq : 0)) * D;
@@ -202,272 +281,292 @@ __global__ void __launch_bounds__(192, 1)
   fence_proxy_async_smem();                             // the tensor cores read these stores
   tc::fence_before();
   __syncthreads();
-  // every CTA of the cluster has its barriers initialised before any remote
-  // arrival (the exits above are the same for the whole cluster)
-  if constexpr (SPLIT > 1) cluster_sync_all();
+  // the barriers of every CTA of the cluster are initialised once all have
+  // arrived; each thread waits for that before its first remote access
+  if constexpr (SPLIT > 1) cluster_arrive();
   tc::fence_after();
   const uint32_t tm = tmem_base;
-  const uint32_t tS = tm;                               // columns [0, 128): S of two tiles
-  const uint32_t tO = tm + 2 * kTcKeys;                 // columns [128, 128 + D): O
+  // TMEM columns: S of group g, buffer b at 64 (2g + b); O of group g at 256 + g D
+  const uint32_t tS = tm;
+  const uint32_t tO = tm + 4 * kTcKeys;
 
-  if (warp == 4) {
-    // ---- producer: K and V tiles through the TMA ring -------------------------------
-    if (lane == 0) {
-      for (int u = 0; u < n_tiles; ++u) {
-        const int t = t_begin + u, st = u % NST;
-        if (u >= NST && !mbar_wait_bounded(&empty_bar[st], ((u / NST) - 1) & 1))
-          atomicOr(p.err, PKV_DEVERR_TIMEOUT);          // keep going: the consumers time out too
-        const int pg0 = t * kTcPages;
-        const int npg = min(kTcPages, n_pages - pg0);
-        mbar_arrive_expect_tx(&full_bar[st], npg * 2 * kBS * D * 2);
-        uint8_t* dst = pKV + st * Cfg::STAGE_BYTES;
-        for (int pg = 0; pg < npg; ++pg) {
-          const int lp = pg0 + pg;
-          int id = p.block_tables[(int64_t)n * p.max_blocks + (lp >> p.ppb_shift)];
-          if (id < 0 || id >= p.num_blocks) {
-            atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
-            id = 0;
-          }
-          const int z = ((id * p.Hkv + h) << p.ppb_shift) + (lp & ((1 << p.ppb_shift) - 1));
-#pragma unroll
-          for (int bx = 0; bx < Cfg::NBOX; ++bx) {
-            uint8_t* kd = dst + bx * Cfg::KV_BOX + pg * (kBS * 128);
-            tma_load_3d(kd, &tmK, &full_bar[st], bx * 64, 0, z);
-            tma_load_3d(kd + Cfg::KV_BYTES, &tmV, &full_bar[st], bx * 64, 0, z);
-          }
-        }
-      }
+  if (warp == 8) {
+    for (int u = NST; u < n_tiles; ++u) {
+      wait(&empty_bar[u % NST], ((u / NST) - 1) & 1);
+      issue(u);
     }
+    __syncwarp();
+    if constexpr (SPLIT > 1) cluster_wait();
     return;
   }
 
   constexpr uint32_t ID_S = tc::idesc_f16(kTcRows, kTcKeys, BF16, false);
   constexpr uint32_t ID_O = tc::idesc_f16(kTcRows, D, BF16, true);
 
-  // S of tile t goes to TMEM buffer t % 2 and P of tile t to shared buffer
-  // t % 2. s_bar[b] (S ready), p_bar[b] (P written) and o_bar[b] (P.V done)
-  // complete once per use of buffer b, so every phase is waited on in order.
-  if (warp == 5) {
-    // ---- MMA warp: S of tile t as soon as its K lands and its S buffer is
-    // free; P.V of tile t - 1 as soon as the softmax has written its P ----------------
+  // Tile u belongs to group g = u % 2 as its j-th tile (j = u / 2): S goes to
+  // TMEM buffer (g, j % 2), P to shared buffer (g, j % 2), P.V accumulates
+  // into O of group g. Each barrier (g, b) completes once per use of its
+  // buffer, so every phase is waited on in order.
+  if (warp == 9) {
+    // ---- MMA warp: S of tile u as soon as its K lands; P.V of tile u - 2 (the
+    // same group's previous tile) once that group has written its P. S of a
+    // buffer is issued after the P.V two uses back, whose P wait covered the
+    // softmax's reads of that buffer. ------------------------------------------
     if (lane == 0) {
-      // u counts this CTA's tiles; buffers and phases follow u
       auto pv = [&](int u) {
-        if (!mbar_wait_bounded(&p_bar[u & 1], (u >> 1) & 1)) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+        const int g = u & 1, j = u >> 1, b = j & 1;
+        wait(&p_bar[g][b], (j >> 1) & 1);
         tc::fence_after();
         const uint32_t vst = sKV + (u % NST) * Cfg::STAGE_BYTES + Cfg::KV_BYTES;
 #pragma unroll
         for (int k = 0; k < kTcKeys / 16; ++k) {
-          const uint64_t a = tc::sdesc(sP + (u & 1) * Cfg::P_BYTES + k * 32, 16, 1024);
-          const uint64_t b = tc::sdesc(vst + k * 2 * 1024, Cfg::KV_BOX, 1024);
-          tc::mma(tO, a, b, ID_O, (u > 0 || k > 0) ? 1u : 0u);
+          const uint64_t a = tc::sdesc(sP + (2 * g + b) * Cfg::P_BYTES + k * 32, 16, 1024);
+          const uint64_t bd = tc::sdesc(vst + k * 2 * 1024, Cfg::KV_BOX, 1024);
+          tc::mma(tO + g * D, a, bd, ID_O, (j > 0 || k > 0) ? 1u : 0u);
         }
-        tc::commit(&o_bar[u & 1]);
+        tc::commit(&o_bar[g][b]);
         tc::commit(&empty_bar[u % NST]);                // the stage is free once these are done
       };
       for (int u = 0; u < n_tiles; ++u) {
-        const int st = u % NST;
-        if (!mbar_wait_bounded(&full_bar[st], (u / NST) & 1)) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+        const int st = u % NST, g = u & 1, j = u >> 1;
+        wait(&full_bar[st], (u / NST) & 1);
         tc::fence_after();
-        // buffer u % 2 was last read by the softmax of tile u - 2, whose P the
-        // P.V of tile u - 2 (issued below, in order) already waited for
         const uint32_t kst = sKV + st * Cfg::STAGE_BYTES;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t ko = (k % 4) * 32u;
           const uint64_t a = tc::sdesc(sQ + (k / 4) * Cfg::Q_BOX + ko, 16, 1024);
-          const uint64_t b = tc::sdesc(kst + (k / 4) * Cfg::KV_BOX + ko, 16, 1024);
-          tc::mma(tS + (u & 1) * kTcKeys, a, b, ID_S, k > 0 ? 1u : 0u);
+          const uint64_t bd = tc::sdesc(kst + (k / 4) * Cfg::KV_BOX + ko, 16, 1024);
+          tc::mma(tS + (2 * g + (j & 1)) * kTcKeys, a, bd, ID_S, k > 0 ? 1u : 0u);
         }
-        tc::commit(&s_bar[u & 1]);
-        if (u > 0) pv(u - 1);
+        tc::commit(&s_bar[g][j & 1]);
+        if (u >= 2) pv(u - 2);
       }
-      if (n_tiles > 0) pv(n_tiles - 1);
+      for (int u = max(0, n_tiles - 2); u < n_tiles; ++u) pv(u);
     }
+    __syncwarp();
+    if constexpr (SPLIT > 1) cluster_wait();
     return;
   }
 
-  // ---- warps 0-3: the softmax, one row per thread --------------------------------
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  // ---- warps 0-7: two softmax groups, one row per thread each ---------------------
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   const int lim = rvalid ? P0 + qi : -1;                // last key this row sees
   const float sl2 = p.qk_scale_log2;
+  const uint32_t tOg = tO + grp * D;
+  const int n_mine = (n_tiles - grp + 1) / 2;           // this group's tiles
   float m_ref = -INFINITY, l = 0.f;
 
-  for (int u = 0; u < n_tiles; ++u) {
+  for (int j = 0; j < n_mine; ++j) {
+    const int u = 2 * j + grp;                          // local tile
     const int t = t_begin + u;                          // key tile
     const int st = u % NST;
-    const int pb = u & 1;
-    if (!mbar_wait_bounded(&s_bar[pb], (u >> 1) & 1)) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+    const int b = j & 1;
+    wait(&s_bar[grp][b], (j >> 1) & 1);
     tc::fence_after();
     uint32_t sv[2][32];
-    tc::ld32(tS + pb * kTcKeys + lane_base, sv[0]);
-    tc::ld32(tS + pb * kTcKeys + lane_base + 32, sv[1]);
+    const uint32_t sbuf = tS + (2 * grp + b) * kTcKeys + lane_base;
+    tc::ld32(sbuf, sv[0]);
+    tc::ld32(sbuf + 32, sv[1]);
     tc::wait_ld();
     // raw scores; keys past this row's causal limit become -inf (only the
     // tiles that cross the limit need the test)
     float x[kTcKeys];
 #pragma unroll
-    for (int j = 0; j < kTcKeys; ++j) x[j] = __uint_as_float(sv[j / 32][j % 32]);
+    for (int c = 0; c < kTcKeys; ++c) x[c] = __uint_as_float(sv[c / 32][c % 32]);
     if (t * kTcKeys + kTcKeys - 1 > lim) {
 #pragma unroll
-      for (int j = 0; j < kTcKeys; ++j)
-        if (t * kTcKeys + j > lim) x[j] = -INFINITY;
+      for (int c = 0; c < kTcKeys; ++c)
+        if (t * kTcKeys + c > lim) x[c] = -INFINITY;
     }
-    float mr = -INFINITY;
+    // row max over 8 independent chains, then a tree
+    float m8[8];
 #pragma unroll
-    for (int j = 0; j < kTcKeys; ++j) mr = fmaxf(mr, x[j]);
-    const float mx = mr * sl2;                          // the scale is positive: max commutes
+    for (int k = 0; k < 8; ++k) m8[k] = x[k];
+#pragma unroll
+    for (int c = 8; c < kTcKeys; ++c) m8[c % 8] = fmaxf(m8[c % 8], x[c]);
+#pragma unroll
+    for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+      for (int k = 0; k < w; ++k) m8[k] = fmaxf(m8[k], m8[k + w]);
+    const float mx = m8[0] * sl2;                       // the scale is positive: max commutes
     // move the reference max only when the row max outgrows it by 2^8
     const bool move = mx > m_ref + kRescaleLog2;
     const float alpha = move ? (m_ref == -INFINITY ? 0.f : ex2_approx(m_ref - mx)) : 1.f;
     if (move) m_ref = mx;
-    if (u > 0 && __any_sync(0xffffffffu, move)) {
-      // O must hold every earlier tile before it is scaled
-      if (!mbar_wait_bounded(&o_bar[(u - 1) & 1], ((u - 1) >> 1) & 1))
-        atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+    if (j > 0 && __any_sync(0xffffffffu, move)) {
+      // O must hold every earlier tile of this group before it is scaled
+      wait(&o_bar[grp][(j - 1) & 1], ((j - 1) >> 1) & 1);
       tc::fence_after();
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t ov[32];
-        tc::ld32(tO + lane_base + c0, ov);
+        tc::ld32(tOg + lane_base + c0, ov);
         tc::wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-        tc::st32(tO + lane_base + c0, ov);
+        for (int c = 0; c < 32; ++c) ov[c] = __float_as_uint(__uint_as_float(ov[c]) * alpha);
+        tc::st32(tOg + lane_base + c0, ov);
       }
       tc::wait_st();
     }
-    if (u >= 2) {
-      // P buffer pb was read by the P.V of tile u - 2
-      if (!mbar_wait_bounded(&o_bar[pb], ((u - 2) >> 1) & 1)) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
-    }
+    // P buffer b was read by the P.V of this group's tile j - 2
+    if (j >= 2) wait(&o_bar[grp][b], ((j - 2) >> 1) & 1);
     const float ms = m_ref == -INFINITY ? 0.f : m_ref;
-    uint8_t* pPb = pP + pb * Cfg::P_BYTES;
-    float rs = 0.f;
+    uint8_t* pPb = pP + (2 * grp + b) * Cfg::P_BYTES;
+    float rs8[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) rs8[k] = 0.f;
 #pragma unroll
     for (int c = 0; c < kTcKeys / 8; ++c) {
       float e[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        e[j] = ex2_approx(fmaf(x[8 * c + j], sl2, -ms));
-        rs += e[j];
+      for (int k = 0; k < 8; ++k) {
+        e[k] = ex2_approx(fmaf(x[8 * c + k], sl2, -ms));
+        rs8[k] += e[k];
       }
       const uint4 w = make_uint4(pack16x2<BF16>(e[0], e[1]), pack16x2<BF16>(e[2], e[3]),
                                  pack16x2<BF16>(e[4], e[5]), pack16x2<BF16>(e[6], e[7]));
       *reinterpret_cast<uint4*>(pPb + swz128(r, c)) = w;
     }
-    l = l * alpha + rs;
+#pragma unroll
+    for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+      for (int k = 0; k < w; ++k) rs8[k] += rs8[k + w];
+    l = l * alpha + rs8[0];
     // V rows with no data for this tile (past the context, or pages not
     // loaded) meet weight 0 in P: zero them so their contents cannot make NaN.
-    // Each warp zeroes a quarter; the P.V waits for every softmax thread.
+    // The group's threads share the rows; the P.V waits for all of them.
     const int vz = loaded_end - t * kTcKeys;
     if (vz < kTcKeys) {
       uint8_t* vtile = pKV + st * Cfg::STAGE_BYTES + Cfg::KV_BYTES;
-      for (int i = tid; i < (kTcKeys - vz) * Cfg::NBOX * 8; i += kTcRows) {
+      for (int i = r; i < (kTcKeys - vz) * Cfg::NBOX * 8; i += kTcRows) {
         const int row = vz + i / (Cfg::NBOX * 8), rest = i % (Cfg::NBOX * 8);
-        const int bx = rest / 8, chunk = rest % 8;
-        *reinterpret_cast<uint4*>(vtile + bx * Cfg::KV_BOX + row * 128 + chunk * 16) =
+        const int bx = rest / 8, chk = rest % 8;
+        *reinterpret_cast<uint4*>(vtile + bx * Cfg::KV_BOX + row * 128 + chk * 16) =
             make_uint4(0u, 0u, 0u, 0u);
       }
     }
     fence_proxy_async_smem();                           // P and the zeros, for the tensor cores
     tc::fence_before();
-    mbar_arrive(&p_bar[pb]);
+    mbar_arrive(&p_bar[grp][b]);
   }
 
-  // ---- epilogue: O / l to the output rows ------------------------------------------
-  if (n_tiles > 0) {
-    // MMAs complete in issue order: the last P.V done means all are
-    const int ul = n_tiles - 1;
-    if (!mbar_wait_bounded(&o_bar[ul & 1], (ul >> 1) & 1)) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+  // ---- epilogue ------------------------------------------------------------------------
+  if (n_mine > 0) {
+    // MMAs complete in issue order: this group's last P.V done means all of its are
+    const int jl = n_mine - 1;
+    wait(&o_bar[grp][jl & 1], (jl >> 1) & 1);
     tc::fence_after();
   }
-  // SPLIT == 2: the follower hands its O row, reference max and sum to the
-  // leader, in the leader's K/V ring (free once the leader's tiles are done):
-  //   O as [D / 4][128 rows] float4 (a warp's rows side by side, no bank
-  //   conflicts), then (m, l) as [128 rows][2] fp32.
-  float m_other = -INFINITY, l_other = 0.f;
+  // The two groups' shares of row r: O_g relative to 2^m_g with sum l_g.
+  // Combined: M = max(m_0, m_1), O = O_0 w_0 + O_1 w_1 with w_g = 2^(m_g - M),
+  // and the same for the sum. (reference max, sum) of each row go through the
+  // group's first P buffer, which its last P.V has finished reading.
+  reinterpret_cast<float2*>(pP + 2 * grp * Cfg::P_BYTES)[r] = make_float2(m_ref, l);
+  named_barrier(1, 2 * kTcRows);
+  const float2 ml0 = reinterpret_cast<const float2*>(pP)[r];
+  const float2 ml1 = reinterpret_cast<const float2*>(pP + 2 * Cfg::P_BYTES)[r];
+  const bool has0 = n_tiles > 0, has1 = n_tiles > 1;   // a group with no tile has no O
+  const float M = fmaxf(ml0.x, ml1.x);
+  const float w0 = has0 && ml0.x != -INFINITY ? ex2_approx(ml0.x - M) : 0.f;
+  const float w1 = has1 && ml1.x != -INFINITY ? ex2_approx(ml1.x - M) : 0.f;
+  const float Lc = ml0.y * w0 + ml1.y * w1;
+
+  // CTA `split` of the cluster finishes columns [split CW, (split + 1) CW),
+  // group g of it the half [g QW, (g + 1) QW) of those.
+  constexpr int CW = D / SPLIT;
+  constexpr int QW = CW / 2;
+  constexpr int CH = QW < 32 ? QW : 32;                 // TMEM columns per load
+  const int mycol = split * CW + grp * QW;
+  // combined O of this CTA for columns [c, c + CH)
+  auto combined = [&](int c, float (&f)[CH]) {
+    uint32_t o0[CH], o1[CH];
+    tmem_ld<CH>(tO + lane_base + c, o0);
+    tmem_ld<CH>(tO + D + lane_base + c, o1);
+    tc::wait_ld();
+#pragma unroll
+    for (int k = 0; k < CH; ++k)
+      f[k] = (w0 != 0.f ? __uint_as_float(o0[k]) * w0 : 0.f) +
+             (w1 != 0.f ? __uint_as_float(o1[k]) * w1 : 0.f);
+  };
+
+  // SPLIT == 2: each CTA hands the other the combined O of the other's
+  // columns, with its M and sum, into the other's K/V ring (drained once that
+  // CTA's last P.V is done):
+  //   O as [CW / 4][128 rows] float4 (a warp's rows side by side, no bank
+  //   conflicts), then (M, sum) as [128 rows] float2.
+  float M_o = -INFINITY, L_o = 0.f;
   const uint32_t recv_rows = sKV;
-  const uint32_t recv_ml = sKV + kTcRows * D * 4;
+  const uint32_t recv_ml = sKV + kTcRows * CW * 4;
   if constexpr (SPLIT > 1) {
-    if (split == 0) {
-      if (tid == 0) mbar_arrive_remote(cluster_map(smem_u32(&ready_bar), 1));
-      if (!mbar_wait_cluster(&recv_bar, 0)) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
-      const float2 ml = *reinterpret_cast<const float2*>(basep + (recv_ml - base) + r * 8);
-      m_other = ml.x;
-      l_other = ml.y;
-    } else {
-      if (!mbar_wait_cluster(&ready_bar, 0)) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
-      const uint32_t dst = cluster_map(recv_rows, 0) + r * 16;
+    const uint32_t other = (uint32_t)(split ^ 1);
+    cluster_wait();                                     // the other CTA's barriers are set up
+    if (tid == 0) mbar_arrive_remote(cluster_map(smem_u32(&ready_bar), other));
+    if (!mbar_wait_cluster(&ready_bar, 0)) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+    const uint32_t dst = cluster_map(recv_rows, other) + r * 16;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t ov[32];
-        tc::ld32(tO + lane_base + c0, ov);
-        tc::wait_ld();
+    for (int c0 = 0; c0 < QW; c0 += CH) {
+      float f[CH];
+      combined((int)other * CW + grp * QW + c0, f);
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const bool has = n_tiles > 0;                  // no tile: nothing accumulated
-          st_cluster_v4(dst + ((c0 + j) / 4) * (kTcRows * 16), has ? __uint_as_float(ov[j]) : 0.f,
-                        has ? __uint_as_float(ov[j + 1]) : 0.f,
-                        has ? __uint_as_float(ov[j + 2]) : 0.f,
-                        has ? __uint_as_float(ov[j + 3]) : 0.f);
-        }
-      }
-      st_cluster_v2(cluster_map(recv_ml, 0) + r * 8, m_ref, l);
-      mbar_arrive_remote(cluster_map(smem_u32(&recv_bar), 0));
+      for (int c = 0; c < CH; c += 4)
+        st_cluster_v4(dst + ((grp * QW + c0 + c) / 4) * (kTcRows * 16), f[c], f[c + 1],
+                      f[c + 2], f[c + 3]);
     }
+    if (grp == 0) st_cluster_v2(cluster_map(recv_ml, other) + r * 8, M, Lc);
+    mbar_arrive_remote(cluster_map(smem_u32(&recv_bar), other));
+    if (!mbar_wait_cluster(&recv_bar, 0)) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+    const float2 ml = *reinterpret_cast<const float2*>(basep + (recv_ml - base) + r * 8);
+    M_o = ml.x;
+    L_o = ml.y;
   }
-  if (split == 0) {
-    // merge the two shares: M = max(m, m'), O = O 2^(m-M) + O' 2^(m'-M)
-    const float M = fmaxf(m_ref, m_other);
-    const float w0 = m_ref == -INFINITY ? 0.f : SPLIT == 1 ? 1.f : ex2_approx(m_ref - M);
-    const float w1 = m_other == -INFINITY ? 0.f : ex2_approx(m_other - M);
-    const float L = l * w0 + l_other * w1;
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    const float a0 = w0 * inv, a1 = w1 * inv;
-    const float4* orecv = reinterpret_cast<const float4*>(basep + (recv_rows - base)) + r;
-    uint16_t* orow = static_cast<uint16_t*>(p.out) + ((int64_t)(q0 + (rvalid ? qi : 0)) * p.Hq +
-                                                      (rvalid ? hq : 0)) * D;
+  // with the other CTA's share: M2 = max(M, M_o), O = O 2^(M - M2) + O_o 2^(M_o - M2)
+  const float M2 = fmaxf(M, M_o);
+  const float a0 = M == -INFINITY ? 0.f : SPLIT == 1 ? 1.f : ex2_approx(M - M2);
+  const float a1 = M_o == -INFINITY ? 0.f : ex2_approx(M_o - M2);
+  const float L2 = Lc * a0 + L_o * a1;
+  const float inv = L2 > 0.f ? 1.f / L2 : 0.f;
+  const float4* orecv = reinterpret_cast<const float4*>(basep + (recv_rows - base)) + r;
+  uint16_t* orow = static_cast<uint16_t*>(p.out) + ((int64_t)(q0 + (rvalid ? qi : 0)) * p.Hq +
+                                                    (rvalid ? hq : 0)) * D;
 #pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 32) {
-      uint32_t ov[32];
-      tc::ld32(tO + lane_base + c0, ov);
-      tc::wait_ld();
-      if (rvalid) {
-        float f[32];
+  for (int c0 = 0; c0 < QW; c0 += CH) {
+    float f[CH];
+    combined(mycol + c0, f);
+    if (rvalid) {
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          float4 o1 = make_float4(0.f, 0.f, 0.f, 0.f);
-          if constexpr (SPLIT > 1) o1 = orecv[((c0 + j) / 4) * kTcRows];
-          f[j] = __uint_as_float(ov[j]) * a0 + o1.x * a1;
-          f[j + 1] = __uint_as_float(ov[j + 1]) * a0 + o1.y * a1;
-          f[j + 2] = __uint_as_float(ov[j + 2]) * a0 + o1.z * a1;
-          f[j + 3] = __uint_as_float(ov[j + 3]) * a0 + o1.w * a1;
-        }
+      for (int c = 0; c < CH; c += 4) {
+        float4 of = make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (SPLIT > 1) of = orecv[((grp * QW + c0 + c) / 4) * kTcRows];
+        f[c] = (f[c] * a0 + of.x * a1) * inv;
+        f[c + 1] = (f[c + 1] * a0 + of.y * a1) * inv;
+        f[c + 2] = (f[c + 2] * a0 + of.z * a1) * inv;
+        f[c + 3] = (f[c + 3] * a0 + of.w * a1) * inv;
+      }
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 w = make_uint4(
-              pack16x2<BF16>(f[8 * c + 0], f[8 * c + 1]), pack16x2<BF16>(f[8 * c + 2], f[8 * c + 3]),
-              pack16x2<BF16>(f[8 * c + 4], f[8 * c + 5]), pack16x2<BF16>(f[8 * c + 6], f[8 * c + 7]));
-          *reinterpret_cast<uint4*>(orow + c0 + 8 * c) = w;
-        }
+      for (int c = 0; c < CH / 8; ++c) {
+        const uint4 w = make_uint4(
+            pack16x2<BF16>(f[8 * c + 0], f[8 * c + 1]), pack16x2<BF16>(f[8 * c + 2], f[8 * c + 3]),
+            pack16x2<BF16>(f[8 * c + 4], f[8 * c + 5]), pack16x2<BF16>(f[8 * c + 6], f[8 * c + 7]));
+        *reinterpret_cast<uint4*>(orow + mycol + c0 + 8 * c) = w;
       }
     }
-    if (rvalid && p.out_lse != nullptr)
-      p.out_lse[(int64_t)(q0 + qi) * p.Hq + hq] = L > 0.f ? (M + log2f(L)) * kLn2 : -INFINITY;
   }
+  if (split == 0 && grp == 0 && rvalid && p.out_lse != nullptr)
+    p.out_lse[(int64_t)(q0 + qi) * p.Hq + hq] = L2 > 0.f ? (M2 + log2f(L2)) * kLn2 : -INFINITY;
   tc::fence_before();
-  named_barrier(1, kTcRows);
+  named_barrier(1, 2 * kTcRows);
   if (warp == 0) tc::dealloc(tm, Cfg::TMEM_COLS);
 }
 
 template <int D, bool BF16, int SPLIT>
 static pkv_status launch_prefill_tc_s(const PrefillParams& q, const CUtensorMap& tmK,
                                       const CUtensorMap& tmV, cudaStream_t stream, int dev) {
-  constexpr int NST = 3;
+  constexpr int NST = 4;
   using Cfg = PrefillTcCfg<D, NST>;
-  static_assert(kTcRows * D * 4 + kTcRows * 8 <= NST * Cfg::STAGE_BYTES,
-                "the follower's rows must fit in the leader's ring");
+  static_assert(Cfg::SMEM_BYTES + 512 <= 227 * 1024, "shared memory (dynamic + static)");
+  static_assert(kTcRows * (D / SPLIT) * 4 + kTcRows * 8 <= NST * Cfg::STAGE_BYTES,
+                "the other CTA's rows must fit in the ring");
   auto kern = prefill_tc_kernel<D, BF16, NST, SPLIT>;
   static bool attr_set[64] = {};
   if (!attr_set[dev]) {
@@ -484,7 +583,7 @@ static pkv_status launch_prefill_tc_s(const PrefillParams& q, const CUtensorMap&
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles * SPLIT, q.Hkv, q.num_seqs);
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = attr;
