@@ -9,8 +9,9 @@
 // tensor cores with its accumulators in tensor memory:
 //
 //   CTA = (query tile, KV head, chunk). Tile rows are (query token, head of
-//   the GQA group) pairs, 128 of them: the MMA M. Warp 8 streams K and V
-//   tiles of 4 pages (64 keys) through a TMA ring. Warp 9 issues
+//   the GQA group) pairs, 128 of them: the MMA M. Warps 8 and 10 stream the
+//   K and the V tiles of 4 pages (64 keys) through two TMA rings. Warp 9
+//   issues, whichever is ready first,
 //     S[128 x 64]  = Q[128 x D] . K_tile^T   (K-major A and B, fp32 in TMEM)
 //   and, once the softmax has written P,
 //     O_g[128 x D] += P[128 x 64] . V_tile   (V read MN-major)
@@ -25,7 +26,7 @@
 //   softmax.
 //
 // Shared memory: Q [D/64][128 rows][128 B], then NST stages of
-// K [D/64][4 pages][16 rows][128 B] and V (same), then four P buffers
+// K [D/64][4 pages][16 rows][128 B], NST stages of V (same), then four P buffers
 // [128 rows][128 B] (two per group; S has two TMEM buffers per group
 // likewise, so the S product of a group's next tile runs while its softmax
 // does), all in the 128-byte swizzled layout (tc.cuh). Placing the four
@@ -39,7 +40,7 @@
 namespace pkv {
 
 constexpr int kTcRows = 128;                  // query rows per CTA (MMA M)
-constexpr int kTcThreads = 320;               // 2 softmax groups of 4 warps, TMA warp, MMA warp
+constexpr int kTcThreads = 352;               // 2 softmax groups of 4 warps, K, MMA and V warps
 constexpr int kTcKeys = 64;                   // keys per tile (S MMA N)
 constexpr int kTcPages = kTcKeys / kBS;
 constexpr float kRescaleLog2 = 8.f;           // reference-max slack (log2 units)
@@ -50,10 +51,10 @@ struct PrefillTcCfg {
   static constexpr int Q_BOX = kTcRows * 128;                // one column block of Q
   static constexpr int Q_BYTES = NBOX * Q_BOX;
   static constexpr int KV_BOX = kTcPages * kBS * 128;        // one column block of a K/V tile
-  static constexpr int KV_BYTES = NBOX * KV_BOX;
-  static constexpr int STAGE_BYTES = 2 * KV_BYTES;
+  static constexpr int KV_BYTES = NBOX * KV_BOX;            // one K (or V) tile
+  static constexpr int RING_BYTES = NST * KV_BYTES;          // one ring (K, then V)
   static constexpr int P_BYTES = kTcRows * 128;              // one P buffer (2 per group)
-  static constexpr int SMEM_BYTES = 1024 + Q_BYTES + NST * STAGE_BYTES + 4 * P_BYTES;
+  static constexpr int SMEM_BYTES = 1024 + Q_BYTES + 2 * RING_BYTES + 4 * P_BYTES;
   static constexpr uint32_t TMEM_COLS = 512;                  // 4 S buffers, 2 O
   static_assert(4 * kTcKeys + 2 * D <= (int)TMEM_COLS, "tensor memory");
 };
@@ -140,8 +141,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
   using Cfg = PrefillTcCfg<D, NST>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ uint64_t full_bar[NST];
-  __shared__ uint64_t empty_bar[NST];
+  // per ring stage: K (or V) tile landed, K (or V) tile read
+  __shared__ uint64_t full_k[NST], empty_k[NST], full_v[NST], empty_v[NST];
   // per softmax group g and buffer b: S ready, P written, P.V done
   __shared__ uint64_t s_bar[2][2], o_bar[2][2], p_bar[2][2];
   __shared__ uint64_t ready_bar, recv_bar;              // cluster hand-off (SPLIT == 2)
@@ -180,10 +181,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* basep = smem_raw + (base - raw);
   const uint32_t sQ = base;
   const uint32_t sKV = base + Cfg::Q_BYTES;
-  const uint32_t sP = sKV + NST * Cfg::STAGE_BYTES;    // [group][buffer] P tiles
+  const uint32_t sV = sKV + Cfg::RING_BYTES;           // V ring after the K ring
+  const uint32_t sP = sV + Cfg::RING_BYTES;            // [group][buffer] P tiles
   uint8_t* pQ = basep;
   uint8_t* pKV = basep + Cfg::Q_BYTES;
-  uint8_t* pP = pKV + NST * Cfg::STAGE_BYTES;
+  uint8_t* pV = pKV + Cfg::RING_BYTES;
+  uint8_t* pP = pV + Cfg::RING_BYTES;
 
   bool failed = false;                                  // a wait ran out: stop waiting
   auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -194,7 +197,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   };
 
-  // ---- producer (warp 8): K and V tiles through the TMA ring. Its lanes look
+  // ---- producers: warp 8 streams K tiles and warp 10 V tiles, each through
+  // its own TMA ring, so a K stage is refilled as soon as its S product is
+  // done and V stages wait only on the P.V products. A producer's lanes look
   // up the page rows 32 pages (8 tiles) at a time, one chunk ahead, so no
   // block-table read waits in front of a TMA issue; lane 0 issues the loads.
   const int pg_begin = t_begin * kTcPages;
@@ -209,6 +214,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     return ((id * p.Hkv + h) << p.ppb_shift) + (lp & ((1 << p.ppb_shift) - 1));
   };
   static_assert(32 % kTcPages == 0, "a tile's pages lie in one chunk");
+  const bool k_warp = warp == 8;
+  const CUtensorMap* tmap = k_warp ? &tmK : &tmV;
+  uint64_t* full_x = k_warp ? full_k : full_v;
+  uint64_t* empty_x = k_warp ? empty_k : empty_v;
+  uint8_t* ring_x = k_warp ? pKV : pV;
   int z_cur = 0, z_next = 0, chunk = 0;
   auto issue = [&](int u) {
     const int t = t_begin + u, st = u % NST;
@@ -219,29 +229,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     const int pg0 = t * kTcPages;
     const int npg = min(kTcPages, n_pages - pg0);
-    if (lane == 0) mbar_arrive_expect_tx(&full_bar[st], npg * 2 * kBS * D * 2);
-    uint8_t* dst = pKV + st * Cfg::STAGE_BYTES;
+    if (lane == 0) mbar_arrive_expect_tx(&full_x[st], npg * kBS * D * 2);
+    uint8_t* dst = ring_x + st * Cfg::KV_BYTES;
     for (int pg = 0; pg < npg; ++pg) {
       const int z = __shfl_sync(0xffffffffu, z_cur, (u * kTcPages + pg) % 32);
       if (lane == 0) {
 #pragma unroll
-        for (int bx = 0; bx < Cfg::NBOX; ++bx) {
-          uint8_t* kd = dst + bx * Cfg::KV_BOX + pg * (kBS * 128);
-          tma_load_3d(kd, &tmK, &full_bar[st], bx * 64, 0, z);
-          tma_load_3d(kd + Cfg::KV_BYTES, &tmV, &full_bar[st], bx * 64, 0, z);
-        }
+        for (int bx = 0; bx < Cfg::NBOX; ++bx)
+          tma_load_3d(dst + bx * Cfg::KV_BOX + pg * (kBS * 128), tmap, &full_x[st], bx * 64, 0, z);
       }
     }
   };
   if (warp == 8) {
-    // the producer sets up the barriers and starts the first tiles right away,
-    // while the other warps load the query tile and allocate tensor memory
+    // the K producer sets up the barriers and starts the first tiles right
+    // away, while the other warps load the query tile and allocate tensor memory
     if (lane == 0) {
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
       for (int s = 0; s < NST; ++s) {
-        mbar_init(&full_bar[s], 1);
-        mbar_init(&empty_bar[s], 1);
+        mbar_init(&full_k[s], 1);
+        mbar_init(&empty_k[s], 1);
+        mbar_init(&full_v[s], 1);
+        mbar_init(&empty_v[s], 1);
       }
       for (int g = 0; g < 2; ++g)
         for (int b = 0; b < 2; ++b) {
@@ -254,10 +263,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       fence_barrier_init();
     }
     __syncwarp();
+  }
+  if (warp == 8 || warp == 10) {
     z_cur = page_row(pg_begin + lane);
     z_next = page_row(pg_begin + 32 + lane);
-    for (int u = 0; u < NST && u < n_tiles; ++u) issue(u);
   }
+  if (warp == 8)
+    for (int u = 0; u < NST && u < n_tiles; ++u) issue(u);
   if (warp == 0) tc::alloc(&tmem_base, Cfg::TMEM_COLS);
 
   // ---- query tile into shared memory (warps 4-7); rows past the chunk are zero ----
@@ -290,9 +302,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tS = tm;
   const uint32_t tO = tm + 4 * kTcKeys;
 
-  if (warp == 8) {
-    for (int u = NST; u < n_tiles; ++u) {
-      wait(&empty_bar[u % NST], ((u / NST) - 1) & 1);
+  if (warp == 8 || warp == 10) {
+    // the V producer starts once the barriers are set up (after the CTA barrier)
+    for (int u = k_warp ? NST : 0; u < n_tiles; ++u) {
+      if (u >= NST) wait(&empty_x[u % NST], ((u / NST) - 1) & 1);
       issue(u);
     }
     __syncwarp();
@@ -308,41 +321,50 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // into O of group g. Each barrier (g, b) completes once per use of its
   // buffer, so every phase is waited on in order.
   if (warp == 9) {
-    // ---- MMA warp: S of tile u as soon as its K lands; P.V of tile u - 2 (the
-    // same group's previous tile) once that group has written its P. S of a
-    // buffer is issued after the P.V two uses back, whose P wait covered the
-    // softmax's reads of that buffer. ------------------------------------------
+    // ---- MMA warp: issues whatever is ready, S products first. S of tile u
+    // needs its K tile landed and its TMEM buffer free: the buffer's previous
+    // tile is u - 4, whose softmax finished reading it before writing the P
+    // that the P.V of u - 4 waited for, so S may run up to four tiles ahead of
+    // the P.V products. P.V of tile u (in order) needs the group's P. ----------
     if (lane == 0) {
-      auto pv = [&](int u) {
-        const int g = u & 1, j = u >> 1, b = j & 1;
-        wait(&p_bar[g][b], (j >> 1) & 1);
-        tc::fence_after();
-        const uint32_t vst = sKV + (u % NST) * Cfg::STAGE_BYTES + Cfg::KV_BYTES;
+      int us = 0, up = 0;                               // next S, next P.V
+      uint32_t idle = 0;
+      while (up < n_tiles && !failed) {
+        if (us < n_tiles && us < up + 4 && mbar_test_wait(&full_k[us % NST], (us / NST) & 1)) {
+          const int g = us & 1, j = us >> 1;
+          tc::fence_after();
+          const uint32_t kst = sKV + (us % NST) * Cfg::KV_BYTES;
 #pragma unroll
-        for (int k = 0; k < kTcKeys / 16; ++k) {
-          const uint64_t a = tc::sdesc(sP + (2 * g + b) * Cfg::P_BYTES + k * 32, 16, 1024);
-          const uint64_t bd = tc::sdesc(vst + k * 2 * 1024, Cfg::KV_BOX, 1024);
-          tc::mma(tO + g * D, a, bd, ID_O, (j > 0 || k > 0) ? 1u : 0u);
-        }
-        tc::commit(&o_bar[g][b]);
-        tc::commit(&empty_bar[u % NST]);                // the stage is free once these are done
-      };
-      for (int u = 0; u < n_tiles; ++u) {
-        const int st = u % NST, g = u & 1, j = u >> 1;
-        wait(&full_bar[st], (u / NST) & 1);
-        tc::fence_after();
-        const uint32_t kst = sKV + st * Cfg::STAGE_BYTES;
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t ko = (k % 4) * 32u;
+            const uint64_t a = tc::sdesc(sQ + (k / 4) * Cfg::Q_BOX + ko, 16, 1024);
+            const uint64_t bd = tc::sdesc(kst + (k / 4) * Cfg::KV_BOX + ko, 16, 1024);
+            tc::mma(tS + (2 * g + (j & 1)) * kTcKeys, a, bd, ID_S, k > 0 ? 1u : 0u);
+          }
+          tc::commit(&s_bar[g][j & 1]);
+          tc::commit(&empty_k[us % NST]);               // the K stage is free once S is done
+          ++us;
+          idle = 0;
+        } else if (up < us && mbar_test_wait(&p_bar[up & 1][(up >> 1) & 1], (up >> 2) & 1) &&
+                   mbar_test_wait(&full_v[up % NST], (up / NST) & 1)) {
+          const int g = up & 1, j = up >> 1, b = j & 1;
+          tc::fence_after();
+          const uint32_t vst = sV + (up % NST) * Cfg::KV_BYTES;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t ko = (k % 4) * 32u;
-          const uint64_t a = tc::sdesc(sQ + (k / 4) * Cfg::Q_BOX + ko, 16, 1024);
-          const uint64_t bd = tc::sdesc(kst + (k / 4) * Cfg::KV_BOX + ko, 16, 1024);
-          tc::mma(tS + (2 * g + (j & 1)) * kTcKeys, a, bd, ID_S, k > 0 ? 1u : 0u);
+          for (int k = 0; k < kTcKeys / 16; ++k) {
+            const uint64_t a = tc::sdesc(sP + (2 * g + b) * Cfg::P_BYTES + k * 32, 16, 1024);
+            const uint64_t bd = tc::sdesc(vst + k * 2 * 1024, Cfg::KV_BOX, 1024);
+            tc::mma(tO + g * D, a, bd, ID_O, (j > 0 || k > 0) ? 1u : 0u);
+          }
+          tc::commit(&o_bar[g][b]);
+          tc::commit(&empty_v[up % NST]);               // the V stage is free once P.V is done
+          ++up;
+          idle = 0;
+        } else if (++idle > (1u << 26)) {
+          failed = true;                                // nothing became ready: give up
+          atomicOr(p.err, PKV_DEVERR_TIMEOUT);
         }
-        tc::commit(&s_bar[g][j & 1]);
-        if (u >= 2) pv(u - 2);
       }
-      for (int u = max(0, n_tiles - 2); u < n_tiles; ++u) pv(u);
     }
     __syncwarp();
     if constexpr (SPLIT > 1) cluster_wait();
@@ -438,7 +460,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // The group's threads share the rows; the P.V waits for all of them.
     const int vz = loaded_end - t * kTcKeys;
     if (vz < kTcKeys) {
-      uint8_t* vtile = pKV + st * Cfg::STAGE_BYTES + Cfg::KV_BYTES;
+      // the V tile has its own barrier: zero its rows only once it has landed
+      wait(&full_v[st], (u / NST) & 1);
+      uint8_t* vtile = pV + st * Cfg::KV_BYTES;
       for (int i = r; i < (kTcKeys - vz) * Cfg::NBOX * 8; i += kTcRows) {
         const int row = vz + i / (Cfg::NBOX * 8), rest = i % (Cfg::NBOX * 8);
         const int bx = rest / 8, chk = rest % 8;
@@ -491,8 +515,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   };
 
   // SPLIT == 2: each CTA hands the other the combined O of the other's
-  // columns, with its M and sum, into the other's K/V ring (drained once that
-  // CTA's last P.V is done):
+  // columns, with its M and sum, into the other's K ring (drained once that
+  // CTA's last P.V, and so its last S, is done):
   //   O as [CW / 4][128 rows] float4 (a warp's rows side by side, no bank
   //   conflicts), then (M, sum) as [128 rows] float2.
   float M_o = -INFINITY, L_o = 0.f;
@@ -565,7 +589,7 @@ static pkv_status launch_prefill_tc_s(const PrefillParams& q, const CUtensorMap&
   constexpr int NST = 4;
   using Cfg = PrefillTcCfg<D, NST>;
   static_assert(Cfg::SMEM_BYTES + 512 <= 227 * 1024, "shared memory (dynamic + static)");
-  static_assert(kTcRows * (D / SPLIT) * 4 + kTcRows * 8 <= NST * Cfg::STAGE_BYTES,
+  static_assert(SPLIT == 1 || kTcRows * (D / SPLIT) * 4 + kTcRows * 8 <= Cfg::RING_BYTES,
                 "the other CTA's rows must fit in the ring");
   auto kern = prefill_tc_kernel<D, BF16, NST, SPLIT>;
   static bool attr_set[64] = {};
