@@ -80,26 +80,40 @@ __global__ void __launch_bounds__((kPrefillConsumers + 1) * 32)
   __syncthreads();
 
   if (warp == kPrefillConsumers) {
-    // ---- producer warp ----------------------------------------------------------
-    if (lane == 0) {
-      for (int t = 0; t < n_tiles; ++t) {
-        const int st = t % NST;
-        if (t >= NST && !mbar_wait_bounded(&empty_bar[st], ((t / NST) - 1) & 1)) {
-          atomicOr(p.err, PKV_DEVERR_TIMEOUT);
-          break;
-        }
-        const int pg0 = t * KT;
-        const int npg = min(KT, n_pages - pg0);
-        mbar_arrive_expect_tx(&full_bar[st], npg * 2 * Geo::PAGE_BYTES);
-        uint8_t* dst = basep + st * STAGE;
-        for (int pg = 0; pg < npg; ++pg) {
-          const int lp = pg0 + pg;                     // logical 16-token page
-          int id = p.block_tables[(int64_t)n * p.max_blocks + (lp >> p.ppb_shift)];
-          if (id < 0 || id >= p.num_blocks) {
-            atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
-            id = 0;
-          }
-          const int z = ((id * p.Hkv + h) << p.ppb_shift) + (lp & ((1 << p.ppb_shift) - 1));
+    // ---- producer warp: its lanes look up the page rows 32 pages at a time,
+    // one chunk ahead, so no block-table read waits in front of a TMA issue;
+    // lane 0 issues the loads ---------------------------------------------------------
+    static_assert(32 % KT == 0, "a tile's pages lie in one chunk");
+    auto page_row = [&](int lp) -> int {
+      if (lp >= n_pages) return 0;
+      int id = p.block_tables[(int64_t)n * p.max_blocks + (lp >> p.ppb_shift)];
+      if (id < 0 || id >= p.num_blocks) {
+        atomicOr(p.err, PKV_DEVERR_BLOCK_ID);
+        id = 0;
+      }
+      return ((id * p.Hkv + h) << p.ppb_shift) + (lp & ((1 << p.ppb_shift) - 1));
+    };
+    int z_cur = page_row(lane), z_next = page_row(32 + lane), chunk = 0;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int st = t % NST;
+      bool ok = t < NST || mbar_wait_bounded(&empty_bar[st], ((t / NST) - 1) & 1);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) {
+        if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+        break;
+      }
+      if ((t * KT) / 32 != chunk) {
+        z_cur = z_next;
+        ++chunk;
+        z_next = page_row(32 * (chunk + 1) + lane);
+      }
+      const int pg0 = t * KT;
+      const int npg = min(KT, n_pages - pg0);
+      if (lane == 0) mbar_arrive_expect_tx(&full_bar[st], npg * 2 * Geo::PAGE_BYTES);
+      uint8_t* dst = basep + st * STAGE;
+      for (int pg = 0; pg < npg; ++pg) {
+        const int z = __shfl_sync(0xffffffffu, z_cur, (pg0 + pg) % 32);
+        if (lane == 0) {
 #pragma unroll
           for (int bx = 0; bx < Geo::NBOX; ++bx) {
             tma_load_3d(dst + pg * Geo::PAGE_BYTES + bx * Geo::BOX_BYTES, &tmK, &full_bar[st],
