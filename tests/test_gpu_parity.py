@@ -266,7 +266,9 @@ def _prefill_case(seed, L, P_, dtype="f16", kv="same", Hq=4, Hkv=2, D=64):
     (1, 40, "f16", "same", 4, 2, 64), (37, 0, "f16", "same", 4, 2, 64),
     (50, 29, "bf16", "same", 8, 2, 128), (23, 17, "bf16", "fp8", 8, 2, 128),
     (100, 300, "bf16", "same", 16, 8, 128), (65, 7, "f16", "fp8", 14, 2, 64),
-    (129, 130, "bf16", "same", 7, 7, 128)])
+    (129, 130, "bf16", "same", 7, 7, 128),
+    (70, 45, "bf16", "same", 28, 4, 128),      # G = 7: 18 tokens, 126 of 128 rows per tile
+    (40, 100, "f16", "same", 16, 1, 64)])      # G = 16: 8 tokens per tile
 def test_prefill_vs_oracle(L, P_, dtype, kv, Hq, Hkv, D):
     c = _prefill_case(9, L, P_, dtype, kv, Hq, Hkv, D)
     kc, vc = product_cache(c)
