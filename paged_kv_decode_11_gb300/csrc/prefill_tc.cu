@@ -40,13 +40,17 @@
 namespace pkv {
 
 constexpr int kTcRows = 128;                  // query rows per CTA (MMA M)
-constexpr int kTcThreads = 352;               // 2 softmax groups of 4 warps, K, MMA and V warps
 constexpr int kTcKeys = 64;                   // keys per tile (S MMA N)
 constexpr int kTcPages = kTcKeys / kBS;
 constexpr float kRescaleLog2 = 8.f;           // reference-max slack (log2 units)
 
+// NG softmax groups of four warps (two up to D = 128; one at D = 256, whose O
+// takes 256 TMEM columns), then the K producer, MMA and V producer warps.
 template <int D, int NST>
 struct PrefillTcCfg {
+  static constexpr int NG = D <= 128 ? 2 : 1;
+  static constexpr int THREADS = NG * kTcRows + 3 * 32;
+  static constexpr int W_K = 4 * NG, W_MMA = 4 * NG + 1, W_V = 4 * NG + 2;
   static constexpr int NBOX = D / 64;                        // 128-byte column blocks per row
   static constexpr int Q_BOX = kTcRows * 128;                // one column block of Q
   static constexpr int Q_BYTES = NBOX * Q_BOX;
@@ -54,9 +58,9 @@ struct PrefillTcCfg {
   static constexpr int KV_BYTES = NBOX * KV_BOX;            // one K (or V) tile
   static constexpr int RING_BYTES = NST * KV_BYTES;          // one ring (K, then V)
   static constexpr int P_BYTES = kTcRows * 128;              // one P buffer (2 per group)
-  static constexpr int SMEM_BYTES = 1024 + Q_BYTES + 2 * RING_BYTES + 4 * P_BYTES;
-  static constexpr uint32_t TMEM_COLS = 512;                  // 4 S buffers, 2 O
-  static_assert(4 * kTcKeys + 2 * D <= (int)TMEM_COLS, "tensor memory");
+  static constexpr int SMEM_BYTES = 1024 + Q_BYTES + 2 * RING_BYTES + 2 * NG * P_BYTES;
+  static constexpr uint32_t TMEM_COLS = 512;                  // 2 S buffers and O per group
+  static_assert(NG * (2 * kTcKeys + D) <= (int)TMEM_COLS, "tensor memory");
 };
 
 __device__ __forceinline__ uint32_t swz128(uint32_t r, uint32_t chunk) {
@@ -136,15 +140,16 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[N]) {
 }
 
 template <int D, bool BF16, int NST, int SPLIT>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(PrefillTcCfg<D, NST>::THREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
   using Cfg = PrefillTcCfg<D, NST>;
+  constexpr int NG = Cfg::NG;
   extern __shared__ uint8_t smem_raw[];
   // per ring stage: K (or V) tile landed, K (or V) tile read
   __shared__ uint64_t full_k[NST], empty_k[NST], full_v[NST], empty_v[NST];
   // per softmax group g and buffer b: S ready, P written, P.V done
-  __shared__ uint64_t s_bar[2][2], o_bar[2][2], p_bar[2][2];
+  __shared__ uint64_t s_bar[NG][2], o_bar[NG][2], p_bar[NG][2];
   __shared__ uint64_t ready_bar, recv_bar;              // cluster hand-off (SPLIT == 2)
   __shared__ uint32_t tmem_base;
 
@@ -214,7 +219,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     return ((id * p.Hkv + h) << p.ppb_shift) + (lp & ((1 << p.ppb_shift) - 1));
   };
   static_assert(32 % kTcPages == 0, "a tile's pages lie in one chunk");
-  const bool k_warp = warp == 8;
+  const bool k_warp = warp == Cfg::W_K;
   const CUtensorMap* tmap = k_warp ? &tmK : &tmV;
   uint64_t* full_x = k_warp ? full_k : full_v;
   uint64_t* empty_x = k_warp ? empty_k : empty_v;
@@ -240,7 +245,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   };
-  if (warp == 8) {
+  if (warp == Cfg::W_K) {
     // the K producer sets up the barriers and starts the first tiles right
     // away, while the other warps load the query tile and allocate tensor memory
     if (lane == 0) {
@@ -252,34 +257,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(&full_v[s], 1);
         mbar_init(&empty_v[s], 1);
       }
-      for (int g = 0; g < 2; ++g)
+      for (int g = 0; g < NG; ++g)
         for (int b = 0; b < 2; ++b) {
           mbar_init(&s_bar[g][b], 1);
           mbar_init(&o_bar[g][b], 1);
           mbar_init(&p_bar[g][b], kTcRows);             // every thread of the group
         }
       mbar_init(&ready_bar, 1);
-      mbar_init(&recv_bar, 2 * kTcRows);
+      mbar_init(&recv_bar, NG * kTcRows);
       fence_barrier_init();
     }
     __syncwarp();
   }
-  if (warp == 8 || warp == 10) {
+  if (warp == Cfg::W_K || warp == Cfg::W_V) {
     z_cur = page_row(pg_begin + lane);
     z_next = page_row(pg_begin + 32 + lane);
   }
-  if (warp == 8)
+  if (warp == Cfg::W_K)
     for (int u = 0; u < NST && u < n_tiles; ++u) issue(u);
   if (warp == 0) tc::alloc(&tmem_base, Cfg::TMEM_COLS);
 
-  // ---- query tile into shared memory (warps 4-7); rows past the chunk are zero ----
-  const int grp = warp >> 2;                            // softmax group (warps 0-7)
+  // ---- query tile into shared memory (the last softmax group); rows past the
+  // chunk are zero ----------------------------------------------------------------
+  const int grp = warp >> 2;                            // softmax group (warps 0 .. 4 NG - 1)
   const int r = tid & (kTcRows - 1);                    // this thread's tile row
   const int rows_used = p.q_tile * G;
   const int qi = i0 + r / G;                            // query token within the chunk
   const int hq = h * G + r % G;                         // query head
   const bool rvalid = r < rows_used && qi < i1;
-  if (grp == 1) {
+  if (grp == NG - 1) {
     const uint16_t* src =
         static_cast<const uint16_t*>(p.q) + ((int64_t)(q0 + (rvalid ? qi : 0)) * p.Hq +
                                              (rvalid ? hq : 0)) * D;
@@ -298,11 +304,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if constexpr (SPLIT > 1) cluster_arrive();
   tc::fence_after();
   const uint32_t tm = tmem_base;
-  // TMEM columns: S of group g, buffer b at 64 (2g + b); O of group g at 256 + g D
+  // TMEM columns: S of group g, buffer b at 64 (2g + b); O of group g at 128 NG + g D
   const uint32_t tS = tm;
-  const uint32_t tO = tm + 4 * kTcKeys;
+  const uint32_t tO = tm + 2 * NG * kTcKeys;
 
-  if (warp == 8 || warp == 10) {
+  if (warp == Cfg::W_K || warp == Cfg::W_V) {
     // the V producer starts once the barriers are set up (after the CTA barrier)
     for (int u = k_warp ? NST : 0; u < n_tiles; ++u) {
       if (u >= NST) wait(&empty_x[u % NST], ((u / NST) - 1) & 1);
@@ -316,22 +322,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   constexpr uint32_t ID_S = tc::idesc_f16(kTcRows, kTcKeys, BF16, false);
   constexpr uint32_t ID_O = tc::idesc_f16(kTcRows, D, BF16, true);
 
-  // Tile u belongs to group g = u % 2 as its j-th tile (j = u / 2): S goes to
+  // Tile u belongs to group g = u % NG as its j-th tile (j = u / NG): S goes to
   // TMEM buffer (g, j % 2), P to shared buffer (g, j % 2), P.V accumulates
   // into O of group g. Each barrier (g, b) completes once per use of its
   // buffer, so every phase is waited on in order.
-  if (warp == 9) {
+  if (warp == Cfg::W_MMA) {
     // ---- MMA warp: issues whatever is ready, S products first. S of tile u
     // needs its K tile landed and its TMEM buffer free: the buffer's previous
-    // tile is u - 4, whose softmax finished reading it before writing the P
-    // that the P.V of u - 4 waited for, so S may run up to four tiles ahead of
-    // the P.V products. P.V of tile u (in order) needs the group's P. ----------
+    // tile is u - 2 NG, whose softmax finished reading it before writing the P
+    // that the P.V of u - 2 NG waited for, so S may run up to 2 NG tiles ahead
+    // of the P.V products. P.V of tile u (in order) needs the group's P. -------
     if (lane == 0) {
       int us = 0, up = 0;                               // next S, next P.V
       uint32_t idle = 0;
       while (up < n_tiles && !failed) {
-        if (us < n_tiles && us < up + 4 && mbar_test_wait(&full_k[us % NST], (us / NST) & 1)) {
-          const int g = us & 1, j = us >> 1;
+        if (us < n_tiles && us < up + 2 * NG &&
+            mbar_test_wait(&full_k[us % NST], (us / NST) & 1)) {
+          const int g = us % NG, j = us / NG;
           tc::fence_after();
           const uint32_t kst = sKV + (us % NST) * Cfg::KV_BYTES;
 #pragma unroll
@@ -345,9 +352,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc::commit(&empty_k[us % NST]);               // the K stage is free once S is done
           ++us;
           idle = 0;
-        } else if (up < us && mbar_test_wait(&p_bar[up & 1][(up >> 1) & 1], (up >> 2) & 1) &&
+        } else if (up < us &&
+                   mbar_test_wait(&p_bar[up % NG][(up / NG) & 1], ((up / NG) >> 1) & 1) &&
                    mbar_test_wait(&full_v[up % NST], (up / NST) & 1)) {
-          const int g = up & 1, j = up >> 1, b = j & 1;
+          const int g = up % NG, j = up / NG, b = j & 1;
           tc::fence_after();
           const uint32_t vst = sV + (up % NST) * Cfg::KV_BYTES;
 #pragma unroll
@@ -371,16 +379,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     return;
   }
 
-  // ---- warps 0-7: two softmax groups, one row per thread each ---------------------
+  // ---- warps 0 .. 4 NG - 1: the softmax groups, one row per thread each ------------
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   const int lim = rvalid ? P0 + qi : -1;                // last key this row sees
   const float sl2 = p.qk_scale_log2;
   const uint32_t tOg = tO + grp * D;
-  const int n_mine = (n_tiles - grp + 1) / 2;           // this group's tiles
+  const int n_mine = (n_tiles - grp + NG - 1) / NG;     // this group's tiles
   float m_ref = -INFINITY, l = 0.f;
 
   for (int j = 0; j < n_mine; ++j) {
-    const int u = 2 * j + grp;                          // local tile
+    const int u = NG * j + grp;                         // local tile
     const int t = t_begin + u;                          // key tile
     const int st = u % NST;
     const int b = j & 1;
@@ -482,36 +490,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     wait(&o_bar[grp][jl & 1], (jl >> 1) & 1);
     tc::fence_after();
   }
-  // The two groups' shares of row r: O_g relative to 2^m_g with sum l_g.
+  // The groups' shares of row r: O_g relative to 2^m_g with sum l_g.
   // Combined: M = max(m_0, m_1), O = O_0 w_0 + O_1 w_1 with w_g = 2^(m_g - M),
   // and the same for the sum. (reference max, sum) of each row go through the
   // group's first P buffer, which its last P.V has finished reading.
   reinterpret_cast<float2*>(pP + 2 * grp * Cfg::P_BYTES)[r] = make_float2(m_ref, l);
-  named_barrier(1, 2 * kTcRows);
+  named_barrier(1, NG * kTcRows);
   const float2 ml0 = reinterpret_cast<const float2*>(pP)[r];
-  const float2 ml1 = reinterpret_cast<const float2*>(pP + 2 * Cfg::P_BYTES)[r];
-  const bool has0 = n_tiles > 0, has1 = n_tiles > 1;   // a group with no tile has no O
+  const float2 ml1 = NG > 1 ? reinterpret_cast<const float2*>(pP + 2 * Cfg::P_BYTES)[r]
+                            : make_float2(-INFINITY, 0.f);
+  // a group with no tile has no O
+  const bool has0 = n_tiles > 0, has1 = NG > 1 && n_tiles > 1;
   const float M = fmaxf(ml0.x, ml1.x);
   const float w0 = has0 && ml0.x != -INFINITY ? ex2_approx(ml0.x - M) : 0.f;
   const float w1 = has1 && ml1.x != -INFINITY ? ex2_approx(ml1.x - M) : 0.f;
   const float Lc = ml0.y * w0 + ml1.y * w1;
 
   // CTA `split` of the cluster finishes columns [split CW, (split + 1) CW),
-  // group g of it the half [g QW, (g + 1) QW) of those.
+  // group g of it the part [g QW, (g + 1) QW) of those.
   constexpr int CW = D / SPLIT;
-  constexpr int QW = CW / 2;
+  constexpr int QW = CW / NG;
   constexpr int CH = QW < 32 ? QW : 32;                 // TMEM columns per load
   const int mycol = split * CW + grp * QW;
   // combined O of this CTA for columns [c, c + CH)
   auto combined = [&](int c, float (&f)[CH]) {
     uint32_t o0[CH], o1[CH];
     tmem_ld<CH>(tO + lane_base + c, o0);
-    tmem_ld<CH>(tO + D + lane_base + c, o1);
+    if constexpr (NG > 1) tmem_ld<CH>(tO + D + lane_base + c, o1);
     tc::wait_ld();
 #pragma unroll
-    for (int k = 0; k < CH; ++k)
-      f[k] = (w0 != 0.f ? __uint_as_float(o0[k]) * w0 : 0.f) +
-             (w1 != 0.f ? __uint_as_float(o1[k]) * w1 : 0.f);
+    for (int k = 0; k < CH; ++k) {
+      f[k] = w0 != 0.f ? __uint_as_float(o0[k]) * w0 : 0.f;
+      if constexpr (NG > 1) f[k] += w1 != 0.f ? __uint_as_float(o1[k]) * w1 : 0.f;
+    }
   };
 
   // SPLIT == 2: each CTA hands the other the combined O of the other's
@@ -579,17 +590,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (split == 0 && grp == 0 && rvalid && p.out_lse != nullptr)
     p.out_lse[(int64_t)(q0 + qi) * p.Hq + hq] = L2 > 0.f ? (M2 + log2f(L2)) * kLn2 : -INFINITY;
   tc::fence_before();
-  named_barrier(1, 2 * kTcRows);
+  named_barrier(1, NG * kTcRows);
   if (warp == 0) tc::dealloc(tm, Cfg::TMEM_COLS);
 }
 
 template <int D, bool BF16, int SPLIT>
 static pkv_status launch_prefill_tc_s(const PrefillParams& q, const CUtensorMap& tmK,
                                       const CUtensorMap& tmV, cudaStream_t stream, int dev) {
-  constexpr int NST = 4;
+  constexpr int NST = D > 128 ? 2 : 4;
   using Cfg = PrefillTcCfg<D, NST>;
   static_assert(Cfg::SMEM_BYTES + 512 <= 227 * 1024, "shared memory (dynamic + static)");
-  static_assert(SPLIT == 1 || kTcRows * (D / SPLIT) * 4 + kTcRows * 8 <= Cfg::RING_BYTES,
+  static_assert(SPLIT == 1 || kTcRows * (D / SPLIT) * 4 + kTcRows * 8 <= 2 * Cfg::RING_BYTES,
                 "the other CTA's rows must fit in the ring");
   auto kern = prefill_tc_kernel<D, BF16, NST, SPLIT>;
   static bool attr_set[64] = {};
@@ -607,7 +618,7 @@ static pkv_status launch_prefill_tc_s(const PrefillParams& q, const CUtensorMap&
   attr[0].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles * SPLIT, q.Hkv, q.num_seqs);
-  cfg.blockDim = dim3(kTcThreads);
+  cfg.blockDim = dim3(Cfg::THREADS);
   cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
   cfg.stream = stream;
   cfg.attrs = attr;
@@ -636,13 +647,16 @@ static pkv_status launch_prefill_tc_t(const PrefillParams& p, const CUtensorMap&
 }
 
 bool prefill_tc_supported(int head_dim, pkv_dtype kv_dtype) {
-  return (head_dim == 64 || head_dim == 128) && kv_dtype != PKV_FP8_E4M3;
+  return (head_dim == 64 || head_dim == 128 || head_dim == 256) && kv_dtype != PKV_FP8_E4M3;
 }
 
 pkv_status launch_prefill_tc(const PrefillParams& p, int head_dim, pkv_dtype kv_dtype,
                              const CUtensorMap& tmK, const CUtensorMap& tmV,
                              cudaStream_t stream, bool may_split) {
   const bool bf = kv_dtype == PKV_BF16;
+  if (head_dim == 256)
+    return bf ? launch_prefill_tc_t<256, true>(p, tmK, tmV, stream, may_split)
+              : launch_prefill_tc_t<256, false>(p, tmK, tmV, stream, may_split);
   if (head_dim == 128)
     return bf ? launch_prefill_tc_t<128, true>(p, tmK, tmV, stream, may_split)
               : launch_prefill_tc_t<128, false>(p, tmK, tmV, stream, may_split);

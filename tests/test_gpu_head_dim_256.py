@@ -83,7 +83,9 @@ def test_rope_cache_bit_exact(rot):
 
 
 @pytest.mark.parametrize("L,P_,kv,Hq,Hkv", [(1, 50, "same", 8, 1), (70, 0, "same", 8, 8),
-                                            (100, 150, "fp8", 16, 2), (33, 47, "same", 16, 2)])
+                                            (100, 150, "fp8", 16, 2), (33, 47, "same", 16, 2),
+                                            (600, 40, "same", 16, 8),   # 80 tiles: no key split
+                                            (200, 330, "same", 4, 4)])  # G = 1, 2-CTA clusters
 def test_prefill_vs_oracle(L, P_, kv, Hq, Hkv):
     c = _case(kv, "bf16", Hq, Hkv, ctx=[30, 60], seed=41, prefill=(L, P_))
     kc, vc = product_cache(c)
