@@ -365,7 +365,8 @@ pkv_status prefill_setup(void* out, const void* q, pkv_dtype q_dtype, const void
 pkv_status prefill_launch(const PrefillCall& c, cudaStream_t stream, bool beside_decode) {
   if (c.empty) return PKV_OK;
   if (prefill_tc_supported(c.head_dim, c.kv_dtype))
-    return launch_prefill_tc(c.p, c.head_dim, c.kv_dtype, c.tmK, c.tmV, stream, !beside_decode);
+    return launch_prefill_tc(c.p, c.head_dim, c.q_dtype, c.kv_dtype, c.tmK, c.tmV, stream,
+                             !beside_decode);
   return launch_prefill(c.p, c.head_dim, c.q_dtype, c.kv_dtype, c.tmK, c.tmV, stream);
 }
 

@@ -99,14 +99,15 @@ pkv_status launch_cache_write(const CacheWriteParams& p, pkv_dtype src_dtype,
 pkv_status launch_rope_cache(const RopeCacheParams& p, pkv_dtype src_dtype, pkv_dtype kv_dtype,
                              cudaStream_t stream);
 
-// Causal chunked prefill on the fifth-generation tensor cores (16-bit caches,
-// head_dim 64 or 128); the other cases take launch_prefill. may_split: the
-// grid may pair two CTAs per query tile (a cluster splitting its keys) when
-// one CTA per tile would leave more than half of the SMs idle.
+// Causal chunked prefill on the fifth-generation tensor cores (16-bit caches
+// at head_dim 64, 128 or 256; E4M3 caches at 64 or 128); the other cases take
+// launch_prefill. may_split: the grid may pair two CTAs per query tile (a
+// cluster splitting its keys) when one CTA per tile would leave more than
+// half of the SMs idle.
 bool prefill_tc_supported(int head_dim, pkv_dtype kv_dtype);
-pkv_status launch_prefill_tc(const PrefillParams& p, int head_dim, pkv_dtype kv_dtype,
-                             const CUtensorMap& tmK, const CUtensorMap& tmV, cudaStream_t stream,
-                             bool may_split);
+pkv_status launch_prefill_tc(const PrefillParams& p, int head_dim, pkv_dtype q_dtype,
+                             pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             cudaStream_t stream, bool may_split);
 
 // Rows of q handled by one prefill CTA for a GQA group size G.
 int prefill_q_tile(int G);

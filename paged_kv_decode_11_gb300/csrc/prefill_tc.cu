@@ -46,7 +46,10 @@ constexpr float kRescaleLog2 = 8.f;           // reference-max slack (log2 units
 
 // NG softmax groups of four warps (two up to D = 128; one at D = 256, whose O
 // takes 256 TMEM columns), then the K producer, MMA and V producer warps.
-template <int D, int NST>
+// KV8: an E4M3 cache. Its tiles land by TMA in an NSS-deep staging ring and
+// the producer warps convert them to f16 (exact: E4M3 is a subset of f16)
+// into the rings the MMAs read.
+template <int D, int NST, bool KV8 = false>
 struct PrefillTcCfg {
   static constexpr int NG = D <= 128 ? 2 : 1;
   static constexpr int THREADS = NG * kTcRows + 3 * 32;
@@ -58,7 +61,11 @@ struct PrefillTcCfg {
   static constexpr int KV_BYTES = NBOX * KV_BOX;            // one K (or V) tile
   static constexpr int RING_BYTES = NST * KV_BYTES;          // one ring (K, then V)
   static constexpr int P_BYTES = kTcRows * 128;              // one P buffer (2 per group)
-  static constexpr int SMEM_BYTES = 1024 + Q_BYTES + 2 * RING_BYTES + 2 * NG * P_BYTES;
+  static constexpr int NSS = KV8 ? 4 : 0;                    // staging stages per operand
+  static constexpr int STG_PAGE = kBS * D;                   // one E4M3 page
+  static constexpr int STG_BYTES = kTcPages * STG_PAGE;      // one staged E4M3 tile
+  static constexpr int SMEM_BYTES =
+      1024 + Q_BYTES + 2 * RING_BYTES + 2 * NG * P_BYTES + 2 * NSS * STG_BYTES;
   static constexpr uint32_t TMEM_COLS = 512;                  // 2 S buffers and O per group
   static_assert(NG * (2 * kTcKeys + D) <= (int)TMEM_COLS, "tensor memory");
 };
@@ -139,15 +146,22 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[N]) {
   else tc::ld16(taddr, v);
 }
 
-template <int D, bool BF16, int NST, int SPLIT>
-__global__ void __launch_bounds__(PrefillTcCfg<D, NST>::THREADS, 1)
+// KV: the cache type; the MMAs take bf16 operands for a bf16 cache and f16
+// ones otherwise (an E4M3 cache is converted to f16, and bf16 queries with
+// it). QBF16: the query and output type.
+template <int D, int KV, bool QBF16, int NST, int SPLIT>
+__global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
-  using Cfg = PrefillTcCfg<D, NST>;
+  constexpr bool KV8 = KV == KV_E4M3;
+  constexpr bool BF16 = KV == KV_BF16;                  // MMA operand type
+  using Cfg = PrefillTcCfg<D, NST, KV8>;
   constexpr int NG = Cfg::NG;
+  constexpr int NSS = Cfg::NSS > 0 ? Cfg::NSS : 1;
   extern __shared__ uint8_t smem_raw[];
-  // per ring stage: K (or V) tile landed, K (or V) tile read
+  // per ring stage: K (or V) tile ready, K (or V) tile read
   __shared__ uint64_t full_k[NST], empty_k[NST], full_v[NST], empty_v[NST];
+  __shared__ uint64_t stg_k[NSS], stg_v[NSS];           // KV8: staged E4M3 tile landed
   // per softmax group g and buffer b: S ready, P written, P.V done
   __shared__ uint64_t s_bar[NG][2], o_bar[NG][2], p_bar[NG][2];
   __shared__ uint64_t ready_bar, recv_bar;              // cluster hand-off (SPLIT == 2)
@@ -192,6 +206,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST>::THREADS, 1)
   uint8_t* pKV = basep + Cfg::Q_BYTES;
   uint8_t* pV = pKV + Cfg::RING_BYTES;
   uint8_t* pP = pV + Cfg::RING_BYTES;
+  uint8_t* pStg = pP + 2 * NG * Cfg::P_BYTES;          // KV8: K staging, then V staging
 
   bool failed = false;                                  // a wait ran out: stop waiting
   auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -223,10 +238,14 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST>::THREADS, 1)
   const CUtensorMap* tmap = k_warp ? &tmK : &tmV;
   uint64_t* full_x = k_warp ? full_k : full_v;
   uint64_t* empty_x = k_warp ? empty_k : empty_v;
+  uint64_t* stg_x = k_warp ? stg_k : stg_v;
   uint8_t* ring_x = k_warp ? pKV : pV;
+  uint8_t* stage_x = pStg + (k_warp ? 0 : NSS * Cfg::STG_BYTES);
   int z_cur = 0, z_next = 0, chunk = 0;
+  // TMA loads of tile u: into ring stage u % NST, or (KV8) into staging
+  // stage u % NSS, one box per E4M3 page
   auto issue = [&](int u) {
-    const int t = t_begin + u, st = u % NST;
+    const int t = t_begin + u;
     if ((u * kTcPages) / 32 != chunk) {
       z_cur = z_next;
       ++chunk;
@@ -234,16 +253,62 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST>::THREADS, 1)
     }
     const int pg0 = t * kTcPages;
     const int npg = min(kTcPages, n_pages - pg0);
-    if (lane == 0) mbar_arrive_expect_tx(&full_x[st], npg * kBS * D * 2);
-    uint8_t* dst = ring_x + st * Cfg::KV_BYTES;
-    for (int pg = 0; pg < npg; ++pg) {
-      const int z = __shfl_sync(0xffffffffu, z_cur, (u * kTcPages + pg) % 32);
-      if (lane == 0) {
+    if constexpr (KV8) {
+      uint64_t* bar = &stg_x[u % NSS];
+      if (lane == 0) mbar_arrive_expect_tx(bar, npg * Cfg::STG_PAGE);
+      uint8_t* dst = stage_x + (u % NSS) * Cfg::STG_BYTES;
+      for (int pg = 0; pg < npg; ++pg) {
+        const int z = __shfl_sync(0xffffffffu, z_cur, (u * kTcPages + pg) % 32);
+        if (lane == 0) tma_load_3d(dst + pg * Cfg::STG_PAGE, tmap, bar, 0, 0, z);
+      }
+    } else {
+      const int st = u % NST;
+      if (lane == 0) mbar_arrive_expect_tx(&full_x[st], npg * kBS * D * 2);
+      uint8_t* dst = ring_x + st * Cfg::KV_BYTES;
+      for (int pg = 0; pg < npg; ++pg) {
+        const int z = __shfl_sync(0xffffffffu, z_cur, (u * kTcPages + pg) % 32);
+        if (lane == 0) {
 #pragma unroll
-        for (int bx = 0; bx < Cfg::NBOX; ++bx)
-          tma_load_3d(dst + bx * Cfg::KV_BOX + pg * (kBS * 128), tmap, &full_x[st], bx * 64, 0, z);
+          for (int bx = 0; bx < Cfg::NBOX; ++bx)
+            tma_load_3d(dst + bx * Cfg::KV_BOX + pg * (kBS * 128), tmap, &full_x[st], bx * 64, 0,
+                        z);
+        }
       }
     }
+  };
+  // KV8: the warp turns staged tile u into f16 in ring stage u % NST (rows
+  // past the loaded keys become zeros), then refills the staging stage
+  auto convert = [&](int u) {
+    using Geo8 = PageGeom<D, KV_E4M3>;
+    constexpr int CPR = D / 16;                          // 16-element chunks per row
+    const int t = t_begin + u, st = u % NST;
+    wait(&stg_x[u % NSS], (u / NSS) & 1);
+    if (u >= NST) wait(&empty_x[st], ((u / NST) - 1) & 1);
+    const uint8_t* src = stage_x + (u % NSS) * Cfg::STG_BYTES;
+    uint8_t* dst = ring_x + st * Cfg::KV_BYTES;
+    const int valid = loaded_end - t * kTcKeys;          // rows of this tile holding keys
+#pragma unroll 4
+    for (int i = lane; i < kTcKeys * CPR; i += 32) {
+      const int row = i / CPR, x = i % CPR;
+      uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+      if (row < valid) {
+        const uint4 e = lds128(smem_u32(src + (row / kBS) * Cfg::STG_PAGE +
+                                        Geo8::row_off(row % kBS, 16 * x)));
+        lo = make_uint4(e4m3x2_to_f16x2(e.x & 0xFFFFu), e4m3x2_to_f16x2(e.x >> 16),
+                        e4m3x2_to_f16x2(e.y & 0xFFFFu), e4m3x2_to_f16x2(e.y >> 16));
+        hi = make_uint4(e4m3x2_to_f16x2(e.z & 0xFFFFu), e4m3x2_to_f16x2(e.z >> 16),
+                        e4m3x2_to_f16x2(e.w & 0xFFFFu), e4m3x2_to_f16x2(e.w >> 16));
+      }
+      // elements 16 x .. 16 x + 15: column block x / 4, 16-byte chunks 2 (x % 4) and + 1
+      uint8_t* d = dst + (x / 4) * Cfg::KV_BOX;
+      *reinterpret_cast<uint4*>(d + swz128(row, 2 * (x % 4))) = lo;
+      *reinterpret_cast<uint4*>(d + swz128(row, 2 * (x % 4) + 1)) = hi;
+    }
+    fence_proxy_async_smem();                            // the tensor cores read these stores
+    mbar_arrive(&full_x[st]);                            // one arrival per lane
+    __syncwarp();
+    fence_proxy_async_smem();                            // before the staging stage is refilled
+    if (u + NSS < n_tiles) issue(u + NSS);
   };
   if (warp == Cfg::W_K) {
     // the K producer sets up the barriers and starts the first tiles right
@@ -252,10 +317,14 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST>::THREADS, 1)
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
       for (int s = 0; s < NST; ++s) {
-        mbar_init(&full_k[s], 1);
+        mbar_init(&full_k[s], KV8 ? 32 : 1);            // KV8: the converting warp's lanes
         mbar_init(&empty_k[s], 1);
-        mbar_init(&full_v[s], 1);
+        mbar_init(&full_v[s], KV8 ? 32 : 1);
         mbar_init(&empty_v[s], 1);
+      }
+      for (int s = 0; s < NSS; ++s) {
+        mbar_init(&stg_k[s], 1);
+        mbar_init(&stg_v[s], 1);
       }
       for (int g = 0; g < NG; ++g)
         for (int b = 0; b < 2; ++b) {
@@ -274,7 +343,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST>::THREADS, 1)
     z_next = page_row(pg_begin + 32 + lane);
   }
   if (warp == Cfg::W_K)
-    for (int u = 0; u < NST && u < n_tiles; ++u) issue(u);
+    for (int u = 0; u < (KV8 ? Cfg::NSS : NST) && u < n_tiles; ++u) issue(u);
   if (warp == 0) tc::alloc(&tmem_base, Cfg::TMEM_COLS);
 
   // ---- query tile into shared memory (the last softmax group); rows past the
@@ -291,8 +360,18 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST>::THREADS, 1)
                                              (rvalid ? hq : 0)) * D;
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
-      const uint4 v = rvalid ? *reinterpret_cast<const uint4*>(src + 8 * c)
-                             : make_uint4(0u, 0u, 0u, 0u);
+      uint4 v = rvalid ? *reinterpret_cast<const uint4*>(src + 8 * c)
+                       : make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (KV8 && QBF16) {
+        // the MMAs run in f16 against an E4M3 cache: round the bf16 query to f16
+        uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+          w[k] = pack_f16x2(f.x, f.y);
+        }
+        v = make_uint4(w[0], w[1], w[2], w[3]);
+      }
       *reinterpret_cast<uint4*>(pQ + (c / 8) * Cfg::Q_BOX + swz128(r, c % 8)) = v;
     }
   }
@@ -310,9 +389,15 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST>::THREADS, 1)
 
   if (warp == Cfg::W_K || warp == Cfg::W_V) {
     // the V producer starts once the barriers are set up (after the CTA barrier)
-    for (int u = k_warp ? NST : 0; u < n_tiles; ++u) {
-      if (u >= NST) wait(&empty_x[u % NST], ((u / NST) - 1) & 1);
-      issue(u);
+    if constexpr (KV8) {
+      if (!k_warp)
+        for (int u = 0; u < Cfg::NSS && u < n_tiles; ++u) issue(u);
+      for (int u = 0; u < n_tiles; ++u) convert(u);
+    } else {
+      for (int u = k_warp ? NST : 0; u < n_tiles; ++u) {
+        if (u >= NST) wait(&empty_x[u % NST], ((u / NST) - 1) & 1);
+        issue(u);
+      }
     }
     __syncwarp();
     if constexpr (SPLIT > 1) cluster_wait();
@@ -382,7 +467,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST>::THREADS, 1)
   // ---- warps 0 .. 4 NG - 1: the softmax groups, one row per thread each ------------
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   const int lim = rvalid ? P0 + qi : -1;                // last key this row sees
-  const float sl2 = p.qk_scale_log2;
+  const float sl2 = p.qk_scale_log2 * (KV8 ? p.k_scales[h] : 1.f);
   const uint32_t tOg = tO + grp * D;
   const int n_mine = (n_tiles - grp + NG - 1) / NG;     // this group's tiles
   float m_ref = -INFINITY, l = 0.f;
@@ -467,7 +552,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST>::THREADS, 1)
     // loaded) meet weight 0 in P: zero them so their contents cannot make NaN.
     // The group's threads share the rows; the P.V waits for all of them.
     const int vz = loaded_end - t * kTcKeys;
-    if (vz < kTcKeys) {
+    if (!KV8 && vz < kTcKeys) {                         // (KV8: zeroed by the conversion)
       // the V tile has its own barrier: zero its rows only once it has landed
       wait(&full_v[st], (u / NST) & 1);
       uint8_t* vtile = pV + st * Cfg::KV_BYTES;
@@ -560,7 +645,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST>::THREADS, 1)
   const float a0 = M == -INFINITY ? 0.f : SPLIT == 1 ? 1.f : ex2_approx(M - M2);
   const float a1 = M_o == -INFINITY ? 0.f : ex2_approx(M_o - M2);
   const float L2 = Lc * a0 + L_o * a1;
-  const float inv = L2 > 0.f ? 1.f / L2 : 0.f;
+  const float inv = L2 > 0.f ? (KV8 ? p.v_scales[h] : 1.f) / L2 : 0.f;
   const float4* orecv = reinterpret_cast<const float4*>(basep + (recv_rows - base)) + r;
   uint16_t* orow = static_cast<uint16_t*>(p.out) + ((int64_t)(q0 + (rvalid ? qi : 0)) * p.Hq +
                                                     (rvalid ? hq : 0)) * D;
@@ -581,8 +666,8 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST>::THREADS, 1)
 #pragma unroll
       for (int c = 0; c < CH / 8; ++c) {
         const uint4 w = make_uint4(
-            pack16x2<BF16>(f[8 * c + 0], f[8 * c + 1]), pack16x2<BF16>(f[8 * c + 2], f[8 * c + 3]),
-            pack16x2<BF16>(f[8 * c + 4], f[8 * c + 5]), pack16x2<BF16>(f[8 * c + 6], f[8 * c + 7]));
+            pack16x2<QBF16>(f[8 * c + 0], f[8 * c + 1]), pack16x2<QBF16>(f[8 * c + 2], f[8 * c + 3]),
+            pack16x2<QBF16>(f[8 * c + 4], f[8 * c + 5]), pack16x2<QBF16>(f[8 * c + 6], f[8 * c + 7]));
         *reinterpret_cast<uint4*>(orow + mycol + c0 + 8 * c) = w;
       }
     }
@@ -594,15 +679,16 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST>::THREADS, 1)
   if (warp == 0) tc::dealloc(tm, Cfg::TMEM_COLS);
 }
 
-template <int D, bool BF16, int SPLIT>
+template <int D, int KV, bool QBF16, int SPLIT>
 static pkv_status launch_prefill_tc_s(const PrefillParams& q, const CUtensorMap& tmK,
                                       const CUtensorMap& tmV, cudaStream_t stream, int dev) {
-  constexpr int NST = D > 128 ? 2 : 4;
-  using Cfg = PrefillTcCfg<D, NST>;
+  constexpr bool KV8 = KV == KV_E4M3;
+  constexpr int NST = (D > 128 || KV8) ? 2 : 4;
+  using Cfg = PrefillTcCfg<D, NST, KV8>;
   static_assert(Cfg::SMEM_BYTES + 512 <= 227 * 1024, "shared memory (dynamic + static)");
   static_assert(SPLIT == 1 || kTcRows * (D / SPLIT) * 4 + kTcRows * 8 <= 2 * Cfg::RING_BYTES,
                 "the other CTA's rows must fit in the ring");
-  auto kern = prefill_tc_kernel<D, BF16, NST, SPLIT>;
+  auto kern = prefill_tc_kernel<D, KV, QBF16, NST, SPLIT>;
   static bool attr_set[64] = {};
   if (!attr_set[dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -629,7 +715,7 @@ static pkv_status launch_prefill_tc_s(const PrefillParams& q, const CUtensorMap&
 // One CTA per query tile when that fills at least half of the GPU (or other
 // work shares it); otherwise a cluster of two per tile, each taking half of
 // the key tiles.
-template <int D, bool BF16>
+template <int D, int KV, bool QBF16>
 static pkv_status launch_prefill_tc_t(const PrefillParams& p, const CUtensorMap& tmK,
                                       const CUtensorMap& tmV, cudaStream_t stream,
                                       bool may_split) {
@@ -642,26 +728,41 @@ static pkv_status launch_prefill_tc_t(const PrefillParams& p, const CUtensorMap&
   PrefillParams q = p;
   q.q_tile = kTcRows / p.G;
   const int64_t ctas = (int64_t)((q.max_q_len + q.q_tile - 1) / q.q_tile) * q.Hkv * q.num_seqs;
-  if (may_split && 2 * ctas <= sms[dev]) return launch_prefill_tc_s<D, BF16, 2>(q, tmK, tmV, stream, dev);
-  return launch_prefill_tc_s<D, BF16, 1>(q, tmK, tmV, stream, dev);
+  if (may_split && 2 * ctas <= sms[dev])
+    return launch_prefill_tc_s<D, KV, QBF16, 2>(q, tmK, tmV, stream, dev);
+  return launch_prefill_tc_s<D, KV, QBF16, 1>(q, tmK, tmV, stream, dev);
+}
+
+template <int D>
+static pkv_status launch_prefill_tc_d(const PrefillParams& p, pkv_dtype q_dtype,
+                                      pkv_dtype kv_dtype, const CUtensorMap& tmK,
+                                      const CUtensorMap& tmV, cudaStream_t stream,
+                                      bool may_split) {
+  if (kv_dtype == PKV_BF16)
+    return launch_prefill_tc_t<D, KV_BF16, true>(p, tmK, tmV, stream, may_split);
+  if (kv_dtype == PKV_F16)
+    return launch_prefill_tc_t<D, KV_F16, false>(p, tmK, tmV, stream, may_split);
+  if constexpr (D <= 128) {
+    return q_dtype == PKV_BF16
+               ? launch_prefill_tc_t<D, KV_E4M3, true>(p, tmK, tmV, stream, may_split)
+               : launch_prefill_tc_t<D, KV_E4M3, false>(p, tmK, tmV, stream, may_split);
+  }
+  return PKV_ERR_UNSUPPORTED;
 }
 
 bool prefill_tc_supported(int head_dim, pkv_dtype kv_dtype) {
-  return (head_dim == 64 || head_dim == 128 || head_dim == 256) && kv_dtype != PKV_FP8_E4M3;
+  if (kv_dtype == PKV_FP8_E4M3) return head_dim == 64 || head_dim == 128;
+  return head_dim == 64 || head_dim == 128 || head_dim == 256;
 }
 
-pkv_status launch_prefill_tc(const PrefillParams& p, int head_dim, pkv_dtype kv_dtype,
-                             const CUtensorMap& tmK, const CUtensorMap& tmV,
+pkv_status launch_prefill_tc(const PrefillParams& p, int head_dim, pkv_dtype q_dtype,
+                             pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
                              cudaStream_t stream, bool may_split) {
-  const bool bf = kv_dtype == PKV_BF16;
   if (head_dim == 256)
-    return bf ? launch_prefill_tc_t<256, true>(p, tmK, tmV, stream, may_split)
-              : launch_prefill_tc_t<256, false>(p, tmK, tmV, stream, may_split);
+    return launch_prefill_tc_d<256>(p, q_dtype, kv_dtype, tmK, tmV, stream, may_split);
   if (head_dim == 128)
-    return bf ? launch_prefill_tc_t<128, true>(p, tmK, tmV, stream, may_split)
-              : launch_prefill_tc_t<128, false>(p, tmK, tmV, stream, may_split);
-  return bf ? launch_prefill_tc_t<64, true>(p, tmK, tmV, stream, may_split)
-            : launch_prefill_tc_t<64, false>(p, tmK, tmV, stream, may_split);
+    return launch_prefill_tc_d<128>(p, q_dtype, kv_dtype, tmK, tmV, stream, may_split);
+  return launch_prefill_tc_d<64>(p, q_dtype, kv_dtype, tmK, tmV, stream, may_split);
 }
 
 }  // namespace pkv

@@ -282,18 +282,20 @@ def test_prefill_vs_oracle(L, P_, dtype, kv, Hq, Hkv, D):
     assert_close(lse, wlse, LSE_TOL, "prefill lse")
 
 
-@pytest.mark.parametrize("L,P_,dtype,Hq,Hkv,D,split", [
-    (640, 100, "f16", 16, 8, 64, False),       # 80 query tiles: one CTA each
-    (300, 500, "bf16", 16, 8, 128, True),      # 40 query tiles: a cluster of two each
-    (200, 0, "bf16", 8, 8, 128, True),         # odd key-tile counts per row
+@pytest.mark.parametrize("L,P_,dtype,Hq,Hkv,D,split,kv", [
+    (640, 100, "f16", 16, 8, 64, False, "same"),    # 80 query tiles: one CTA each
+    (300, 500, "bf16", 16, 8, 128, True, "same"),   # 40 query tiles: a cluster of two each
+    (200, 0, "bf16", 8, 8, 128, True, "same"),      # odd key-tile counts per row
+    (640, 100, "bf16", 16, 8, 128, False, "fp8"),   # E4M3 tiles converted on chip
+    (300, 500, "f16", 16, 8, 64, True, "fp8"),
 ])
-def test_prefill_one_cta_and_cluster_key_split(L, P_, dtype, Hq, Hkv, D, split):
+def test_prefill_one_cta_and_cluster_key_split(L, P_, dtype, Hq, Hkv, D, split, kv):
     # the tensor-core prefill splits each query tile's keys over a cluster of
     # two CTAs when the tiles alone would fill at most half of the SMs
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     ctas = -(-L // (128 // (Hq // Hkv))) * Hkv
     assert (2 * ctas <= sms) == split, "case does not take the intended path"
-    c = _prefill_case(12, L, P_, dtype, "same", Hq, Hkv, D)
+    c = _prefill_case(12, L, P_, dtype, kv, Hq, Hkv, D)
     kc, vc = product_cache(c)
     out, lse = run_prefill(c, kc, vc)
     check_device_ok()
