@@ -196,8 +196,10 @@ pkv_status paged_attn_decode_noalloc(void* out, const void* q, pkv_dtype q_dtype
  *   out_lse: optional fp32 [total_q_tokens, Hq].
  *   A chunk with L_n > seq_lens[n] sets PKV_DEVERR_QLEN and is skipped.
  *   Launch: one CTA per tile of query rows; when those would occupy at most
- *   half of the SMs (16-bit caches, D 64 or 128), a cluster of two CTAs per
- *   tile, each over half of the tile's keys, merged by log-sum-exp on chip.
+ *   half of the SMs, a cluster of two CTAs per tile, each over half of the
+ *   tile's keys, merged by log-sum-exp on chip (tensor-core kernel: 16-bit
+ *   caches at D 64/128/256, E4M3 caches at D 64/128). With an E4M3 cache a
+ *   bf16 q is rounded to f16 for the MMAs (exact for |q| in [2^-14, 65504]).
  */
 pkv_status paged_attn_prefill_chunk(void* out, const void* q,
                                     pkv_dtype q_dtype, const void* k_cache,
