@@ -285,24 +285,29 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
     wait(&stg_x[u % NSS], (u / NSS) & 1);
     if (u >= NST) wait(&empty_x[st], ((u / NST) - 1) & 1);
     const uint8_t* src = stage_x + (u % NSS) * Cfg::STG_BYTES;
-    uint8_t* dst = ring_x + st * Cfg::KV_BYTES;
     const int valid = loaded_end - t * kTcKeys;          // rows of this tile holding keys
-#pragma unroll 4
-    for (int i = lane; i < kTcKeys * CPR; i += 32) {
-      const int row = i / CPR, x = i % CPR;
-      uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-      if (row < valid) {
-        const uint4 e = lds128(smem_u32(src + (row / kBS) * Cfg::STG_PAGE +
-                                        Geo8::row_off(row % kBS, 16 * x)));
-        lo = make_uint4(e4m3x2_to_f16x2(e.x & 0xFFFFu), e4m3x2_to_f16x2(e.x >> 16),
-                        e4m3x2_to_f16x2(e.y & 0xFFFFu), e4m3x2_to_f16x2(e.y >> 16));
-        hi = make_uint4(e4m3x2_to_f16x2(e.z & 0xFFFFu), e4m3x2_to_f16x2(e.z >> 16),
-                        e4m3x2_to_f16x2(e.w & 0xFFFFu), e4m3x2_to_f16x2(e.w >> 16));
-      }
-      // elements 16 x .. 16 x + 15: column block x / 4, 16-byte chunks 2 (x % 4) and + 1
-      uint8_t* d = dst + (x / 4) * Cfg::KV_BOX;
-      *reinterpret_cast<uint4*>(d + swz128(row, 2 * (x % 4))) = lo;
-      *reinterpret_cast<uint4*>(d + swz128(row, 2 * (x % 4) + 1)) = hi;
+    // lane = (row in a group of RPI rows, 16-element chunk x of the row): x is
+    // fixed per lane, so the chunk's column block and swizzle slot are too
+    constexpr int RPI = 32 / CPR;
+    const int x = lane % CPR, rsub = lane / CPR;
+    uint8_t* dcol = ring_x + st * Cfg::KV_BYTES + (x / 4) * Cfg::KV_BOX;
+    const int c16 = 2 * (x % 4);
+#pragma unroll
+    for (int k = 0; k < kTcKeys / RPI; ++k) {
+      const int row = k * RPI + rsub;
+      // rows of pages not loaded hold stale bytes: read anyway, zero below
+      const uint4 e = *reinterpret_cast<const uint4*>(src + (row / kBS) * Cfg::STG_PAGE +
+                                                      Geo8::row_off(row % kBS, 16 * x));
+      const bool keep = row < valid;
+      const uint4 lo = keep ? make_uint4(e4m3x2_to_f16x2(e.x & 0xFFFFu), e4m3x2_to_f16x2(e.x >> 16),
+                                         e4m3x2_to_f16x2(e.y & 0xFFFFu), e4m3x2_to_f16x2(e.y >> 16))
+                            : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 hi = keep ? make_uint4(e4m3x2_to_f16x2(e.z & 0xFFFFu), e4m3x2_to_f16x2(e.z >> 16),
+                                         e4m3x2_to_f16x2(e.w & 0xFFFFu), e4m3x2_to_f16x2(e.w >> 16))
+                            : make_uint4(0u, 0u, 0u, 0u);
+      // elements 16 x .. 16 x + 15: 16-byte chunks c16 and c16 + 1 of the row
+      *reinterpret_cast<uint4*>(dcol + swz128(row, c16)) = lo;
+      *reinterpret_cast<uint4*>(dcol + swz128(row, c16 + 1)) = hi;
     }
     fence_proxy_async_smem();                            // the tensor cores read these stores
     mbar_arrive(&full_x[st]);                            // one arrival per lane
