@@ -38,6 +38,7 @@ from workloads import BENCH_CONFIG, CONFIGS, empty_cache, make_case  # noqa: E40
 
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 256 << 20
 CLOCK_QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -61,6 +62,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work budget of the oracle baseline sample")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time the workload's prefill chunk alone (paged_attn_prefill_chunk); "
+                         "prints a TFLOP/s line instead of the step line")
     return ap.parse_args()
 
 
@@ -216,7 +220,8 @@ def workload_desc(case) -> str:
          f"paged decode attention, B{case.B} Hq{case.Hq} Hkv{case.Hkv} D{case.D} block 16, "
          f"{ctxs}, {case.dtype} q, {kv}, pool {case.num_blocks} blocks")
     if case.prefill is not None:
-        s += f" + prefill chunk L{case.prefill.L} on P{case.prefill.P} (second stream)"
+        s += (f" + prefill chunk L{case.prefill.L} on P{case.prefill.P} (one paged_attn_varlen "
+              f"call with the decode rows)")
     if cfg.get("shared_prefix"):
         s += f"; {cfg['shared_prefix'][0]} seqs share a {cfg['shared_prefix'][1]}-token prefix"
     return s
@@ -401,7 +406,7 @@ def run_ours(args):
             "dtype": (("e4m3 KV dequantised to f16 for m16n8k16 MMA, fp32 accumulate"
                        if case.kv_fp8 else f"{case.dtype} m16n8k16 MMA, fp32 accumulate")
                       + ("; prefill chunk on tcgen05 MMA (TMEM fp32 accumulators)"
-                         if case.prefill is not None and not case.kv_fp8 else "")),
+                         if case.prefill is not None else "")),
             "data": "synthetic (seeded N(0,1) values, random block placement)",
             "config": {
                 "workload": workload_desc(case),
@@ -582,10 +587,112 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ---- the prefill chunk alone ----------------------------------------------------------
+
+def prefill_flops(case) -> float:
+    """Causal attention flops of the chunk: row i of L sees P + i + 1 keys; QK^T and PV
+    each take 2 flops per multiply-add."""
+    pf = case.prefill
+    keys = sum(pf.P + i + 1 for i in range(pf.L))
+    return 4.0 * case.Hq * case.D * keys
+
+
+def measured_bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (bf16 burst)"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def run_prefill_only(args):
+    """paged_attn_prefill_chunk on the workload's chunk, timed alone with CUDA events on
+    its stream (L2 flushed between calls, untimed); tensor-core roofline."""
+    rank, world, local = dist_setup()
+    torch.cuda.set_device(local)
+    from paged_kv_decode_11_gb300 import build as pkv_build
+    pkv_build.build()
+    import paged_kv_decode_11_gb300 as P
+    from paged_kv_decode_11_gb300.step import MixedStep
+    P.load()
+    case = make_case(args.config, args.seed + rank, device="cuda")
+    if case.prefill is None:
+        raise SystemExit(f"--prefill-only: workload {args.config} has no prefill chunk")
+    kc, vc = empty_cache(case, "cuda")
+    ks = vs = None
+    if case.kv_fp8:
+        ks = torch.from_numpy(case.k_scales).cuda()
+        vs = torch.from_numpy(case.v_scales).cuda()
+    P.reshape_and_cache(case.fill_k, case.fill_v, kc, vc,
+                        torch.from_numpy(case.fill_slots).cuda(), ks, vs)
+    P.reshape_and_cache(case.new_k, case.new_v, kc, vc,
+                        torch.from_numpy(case.new_slots).cuda(), ks, vs)
+    step = MixedStep.from_case(case, kc, vc, mode="streams")
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        step.prefill(stream)
+    torch.cuda.synchronize()
+    assert P.pkv_get_device_error() == 0
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        step.prefill(stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    rows = sampler.stop() if rank == 0 else []
+    assert P.pkv_get_device_error() == 0
+    ms = allreduce(float(np.mean([a.elapsed_time(b) for a, b in ev])), "max", world)
+    flops = prefill_flops(case)
+    value = allreduce(flops, "sum", world) / (ms / 1e3) / 1e12
+    peak, peak_kind = measured_bf16_peak()
+    achieved = flops / (ms / 1e3) / 1e12
+    if rank == 0:
+        pf = case.prefill
+        print(json.dumps({
+            "metric": "causal chunked prefill: TFLOP/s (attention flops of the chunk)",
+            "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": ("f16" if case.kv_fp8 or case.dtype == "f16" else "bf16")
+                     + " tcgen05 MMA operands, fp32 TMEM accumulators",
+            "data": "synthetic (seeded N(0,1) values, random block placement)",
+            "config": {"workload": f"{case.name} prefill chunk alone: L{pf.L} on P{pf.P}, "
+                                   f"Hq{case.Hq} Hkv{case.Hkv} D{case.D}, "
+                                   f"{'E4M3' if case.kv_fp8 else case.dtype} KV, "
+                                   f"{case.dtype} q, block 16",
+                       "flops_per_call": flops,
+                       "l2": f"flushed between timed calls ({L2_FLUSH_BYTES >> 20} MiB write, "
+                             f"untimed)"},
+            "roofline": {"kernel": "prefill_tc_kernel (one launch per call)", "bound": "tensor",
+                         "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None},
+            "clocks": ClockSampler.summarise(rows, t0, t1),
+            "gpu_launches": K,
+        }), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.prefill_only:
+        run_prefill_only(args)
     else:
         run_ours(args)
 

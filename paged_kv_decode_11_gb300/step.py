@@ -158,6 +158,15 @@ class MixedStep:
         self.ev_prefill.record(self.side)
         main.wait_event(self.ev_prefill)
 
+    def prefill(self, stream: Optional[torch.cuda.Stream] = None):
+        """The chunk alone through paged_attn_prefill_chunk (the cache already holds it)."""
+        d = self.decode
+        B.paged_attn_prefill_chunk(self.prefill_out, self.pf_q, d.k_cache, d.v_cache,
+                                   self.pf_block_tables, self.pf_seq_lens, self.pf_cu_q_lens,
+                                   d.scale, self.pf_max_q_len, d.k_scales, d.v_scales,
+                                   out_lse=self.prefill_lse,
+                                   stream=stream or torch.cuda.current_stream())
+
     def inputs(self):
         d = self.decode
         if self.mode == "varlen":
