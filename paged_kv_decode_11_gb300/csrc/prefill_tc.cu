@@ -1,5 +1,6 @@
 // prefill_tc.cu — causal chunked-prefill attention on the fifth-generation
-// tensor cores (tcgen05), for 16-bit caches at head_dim 64 and 128.
+// tensor cores (tcgen05): 16-bit caches at head_dim 64, 128 and 256, E4M3
+// caches at 64 and 128.
 //
 // Follows "Chunked Prefill" (Litellama, Features: a long prompt enters the
 // batch as chunks of new query tokens attending their cached context) with
@@ -9,29 +10,32 @@
 // tensor cores with its accumulators in tensor memory:
 //
 //   CTA = (query tile, KV head, chunk). Tile rows are (query token, head of
-//   the GQA group) pairs, 128 of them: the MMA M. Warps 8 and 10 stream the
-//   K and the V tiles of 4 pages (64 keys) through two TMA rings. Warp 9
-//   issues, whichever is ready first,
+//   the GQA group) pairs, 128 of them: the MMA M. Two producer warps stream
+//   the K and the V tiles of 4 pages (64 keys) through two TMA rings (for an
+//   E4M3 cache through a staging ring, converting each tile to f16). One
+//   MMA warp issues, whichever is ready first,
 //     S[128 x 64]  = Q[128 x D] . K_tile^T   (K-major A and B, fp32 in TMEM)
 //   and, once the softmax has written P,
 //     O_g[128 x D] += P[128 x 64] . V_tile   (V read MN-major)
-//   Two softmax groups of four warps take the key tiles in turn (group g the
-//   tiles u with u % 2 == g), each with its own S buffers, P buffers and O
-//   accumulator, so one group's softmax runs while the other waits on the
-//   tensor cores. In a group, warp w owns TMEM lanes 32 (w % 4) ..: thread r
-//   holds row r of S, so the row max and sum need no shuffles. O_g and the
-//   row sum are kept relative to a reference max that moves only when the
-//   row max grows by more than 2^8, so O in TMEM is rescaled rarely. At the
-//   end the two groups' (O, max, sum) are merged by log-sum-exp, the same
-//   softmax.
+//   Softmax groups of four warps take the key tiles in turn (two groups up to
+//   D = 128: group g the tiles u with u % 2 == g; one at D = 256), each with
+//   its own S buffers, P buffers and O accumulator, so one group's softmax
+//   runs while the other waits on the tensor cores. In a group, warp w owns
+//   TMEM lanes 32 (w % 4) ..: thread r holds row r of S, so the row max and
+//   sum need no shuffles. O_g and the row sum are kept relative to a
+//   reference max that moves only when the row max grows by more than 2^8,
+//   so O in TMEM is rescaled rarely. At the end the groups' (O, max, sum)
+//   are merged by log-sum-exp, the same softmax. When a small grid leaves
+//   SMs idle, a cluster of two CTAs splits each tile's keys and the two
+//   merge the same way through distributed shared memory.
 //
 // Shared memory: Q [D/64][128 rows][128 B], then NST stages of
-// K [D/64][4 pages][16 rows][128 B], NST stages of V (same), then four P buffers
-// [128 rows][128 B] (two per group; S has two TMEM buffers per group
+// K [D/64][4 pages][16 rows][128 B], NST stages of V (same), then two P
+// buffers [128 rows][128 B] per group (S has two TMEM buffers per group
 // likewise, so the S product of a group's next tile runs while its softmax
-// does), all in the 128-byte swizzled layout (tc.cuh). Placing the four
-// pages of a 64-byte column block back to back gives every operand a
-// uniform 1 KB stride between 8-row groups.
+// does), all in the 128-byte swizzled layout (tc.cuh), then (E4M3) the K and
+// V staging rings. Placing the four pages of a 64-byte column block back to
+// back gives every operand a uniform 1 KB stride between 8-row groups.
 #include <cuda.h>
 #include "common.cuh"
 #include "launch.h"
@@ -189,7 +193,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
   const int n_pages = (key_end + kBS - 1) / kBS;
   const int n_tiles_all = (key_end + kTcKeys - 1) / kTcKeys;
   // this CTA's share of the key tiles: [t_begin, t_begin + n_tiles); its
-  // local tile u goes to softmax group u % 2
+  // local tile u goes to softmax group u % NG
   const int per_split = (n_tiles_all + SPLIT - 1) / SPLIT;
   const int t_begin = split * per_split;
   const int n_tiles = max(0, min(n_tiles_all, t_begin + per_split) - t_begin);
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
     }
   };
 
-  // ---- producers: warp 8 streams K tiles and warp 10 V tiles, each through
+  // ---- producers: warp W_K streams K tiles and warp W_V V tiles, each through
   // its own TMA ring, so a K stage is refilled as soon as its S product is
   // done and V stages wait only on the P.V products. A producer's lanes look
   // up the page rows 32 pages (8 tiles) at a time, one chunk ahead, so no
