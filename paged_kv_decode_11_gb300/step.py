@@ -27,6 +27,24 @@ def _dev(a, device="cuda"):
     return a.to(device).contiguous()
 
 
+def _pack(obj, names):
+    """Moves the named tensor attributes of obj into one device buffer (each
+    at a 256-byte aligned offset) and points the attributes at views of it,
+    so a step's inputs arrive with one host-to-device copy. Returns the buffer."""
+    ts = [getattr(obj, n) for n in names]
+    offs, total = [], 0
+    for t in ts:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) & ~255
+    buf = torch.empty(max(total, 256), dtype=torch.uint8, device=ts[0].device)
+    for n, t, o in zip(names, ts, offs):
+        nb = t.numel() * t.element_size()
+        v = buf[o:o + nb].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        setattr(obj, n, v)
+    return buf
+
+
 class DecodeStep:
     """Device-resident inputs of one decode step and its outputs."""
 
@@ -45,6 +63,8 @@ class DecodeStep:
         ws = B.paged_attn_decode_workspace_size(Bn, Hq, k_cache.shape[1], D, self.max_seq_len,
                                                 self.partition_tokens)
         self.workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=q.device)
+        self.in_buf = _pack(self, ["q", "new_k", "new_v", "new_slots", "block_tables",
+                                   "seq_lens"])
 
     @classmethod
     def from_case(cls, case, k_cache, v_cache):
@@ -70,9 +90,10 @@ class DecodeStep:
         self.write_cache(stream)
         self.attend(stream)
 
-    # host <-> device traffic of one step, for end-to-end timing
+    # host <-> device traffic of one step, for end-to-end timing: the inputs
+    # live in one buffer, so one copy brings them all
     def inputs(self):
-        return [self.q, self.new_k, self.new_v, self.new_slots, self.block_tables, self.seq_lens]
+        return [self.in_buf]
 
     def outputs(self):
         return [self.out]
@@ -115,12 +136,16 @@ class MixedStep:
                                   pf_cu_q_lens.to(torch.int32) + nd]).contiguous()
             self.prefill_out = self.out_all[nd:]
             self.prefill_lse = self.lse_all[nd:]
+            self.in_buf = _pack(self, ["q_all", "all_new_k", "all_new_v", "all_new_slots",
+                                       "bt_all", "seq_lens_all", "qsl"])
         else:
             self.prefill_out = torch.empty_like(pf_q)
             self.prefill_lse = torch.empty(pf_q.shape[:2], dtype=torch.float32, device=dev)
             self.side = torch.cuda.Stream(device=dev)
             self.ev_written = torch.cuda.Event()
             self.ev_prefill = torch.cuda.Event()
+            self.in_buf = _pack(self, ["all_new_k", "all_new_v", "all_new_slots", "pf_q",
+                                       "pf_block_tables", "pf_seq_lens", "pf_cu_q_lens"])
 
     @classmethod
     def from_case(cls, case, k_cache, v_cache, mode: str = "varlen"):
@@ -168,12 +193,9 @@ class MixedStep:
                                    stream=stream or torch.cuda.current_stream())
 
     def inputs(self):
-        d = self.decode
         if self.mode == "varlen":
-            return [self.q_all, self.all_new_k, self.all_new_v, self.all_new_slots, self.bt_all,
-                    self.seq_lens_all, self.qsl]
-        return [d.q, self.all_new_k, self.all_new_v, self.all_new_slots, d.block_tables,
-                d.seq_lens, self.pf_q, self.pf_block_tables, self.pf_seq_lens, self.pf_cu_q_lens]
+            return [self.in_buf]
+        return [self.decode.in_buf, self.in_buf]
 
     def outputs(self):
         if self.mode == "varlen":
