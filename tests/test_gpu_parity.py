@@ -330,6 +330,23 @@ def test_prefill_several_sequences_in_one_call():
     assert_close(out, want, 1e-2, "multi-seq prefill")
 
 
+@pytest.mark.parametrize("kv", ["same", "fp8"])
+def test_prefill_flags_bad_block_id(kv):
+    # an id past the pool is flagged and read as block 0: the call completes
+    c = _prefill_case(13, 100, 60, "bf16", kv, 8, 2, 128)
+    kc, vc = product_cache(c)
+    pf = c.prefill
+    bt = pf.block_tables.copy()
+    bt[0, 3] = c.num_blocks
+    q = dev(pf.q)
+    out = torch.zeros_like(q)
+    ks, vs = scales(c)
+    P.paged_attn_prefill_chunk(out, q, kc, vc, dev(bt), dev(pf.seq_lens), dev(pf.cu_q_lens),
+                               float(c.scale), pf.L, ks, vs)
+    torch.cuda.synchronize()
+    assert P.pkv_get_device_error() & 0x1
+
+
 def test_prefill_flags_chunk_longer_than_context():
     c = _prefill_case(11, 8, 4)
     kc, vc = product_cache(c)
