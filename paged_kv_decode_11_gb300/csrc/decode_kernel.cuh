@@ -461,7 +461,7 @@ static pkv_status launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK,
   auto kern = decode_kernel<D, KV, QBF16, NT, NW, NST, GATHER>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // per device; the call is idempotent
   if (!attr_set[dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg::SMEM_BYTES) != cudaSuccess)

@@ -268,9 +268,8 @@ static pkv_status launch_prefill_t(const PrefillParams& p, const CUtensorMap& tm
   using Cfg = PrefillCfg<D, KV, NST, KT>;
   auto kern = prefill_chunk_kernel<D, KV, QBF16, NST, KT>;
   int dev = 0;
-  cudaGetDevice(&dev);
-  static bool attr_set[64] = {};
-  if (dev < 0 || dev >= 64) return PKV_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
+  static std::atomic<bool> attr_set[64];  // per device; the call is idempotent
   if (!attr_set[dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg::SMEM_BYTES) != cudaSuccess)

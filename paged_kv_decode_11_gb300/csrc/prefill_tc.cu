@@ -698,7 +698,7 @@ static pkv_status launch_prefill_tc_s(const PrefillParams& q, const CUtensorMap&
   static_assert(SPLIT == 1 || kTcRows * (D / SPLIT) * 4 + kTcRows * 8 <= 2 * Cfg::RING_BYTES,
                 "the other CTA's rows must fit in the ring");
   auto kern = prefill_tc_kernel<D, KV, QBF16, NST, SPLIT>;
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // per device; the call is idempotent
   if (!attr_set[dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg::SMEM_BYTES) != cudaSuccess)
@@ -730,14 +730,17 @@ static pkv_status launch_prefill_tc_t(const PrefillParams& p, const CUtensorMap&
                                       bool may_split) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
-  static int sms[64] = {};
-  if (sms[dev] == 0 &&
-      cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return PKV_ERR_CUDA;
+  static std::atomic<int> sms[64];                      // per device SM count, read once
+  int n_sms = sms[dev].load();
+  if (n_sms == 0) {
+    if (cudaDeviceGetAttribute(&n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    sms[dev].store(n_sms);
+  }
   PrefillParams q = p;
   q.q_tile = kTcRows / p.G;
   const int64_t ctas = (int64_t)((q.max_q_len + q.q_tile - 1) / q.q_tile) * q.Hkv * q.num_seqs;
-  if (may_split && 2 * ctas <= sms[dev])
+  if (may_split && 2 * ctas <= n_sms)
     return launch_prefill_tc_s<D, KV, QBF16, 2>(q, tmK, tmV, stream, dev);
   return launch_prefill_tc_s<D, KV, QBF16, 1>(q, tmK, tmV, stream, dev);
 }
