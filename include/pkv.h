@@ -233,11 +233,12 @@ pkv_status paged_attn_prefill_chunk(void* out, const void* q,
  *   workspace is paged_attn_decode_workspace_size(num_decode_seqs, Hq, Hkv,
  *   D, max_decode_seq_len, partition_tokens) bytes), chunk rows exactly as
  *   paged_attn_prefill_chunk computes them (max_q_len bounds every chunk).
- *   Everything is enqueued on `stream`: the split-KV counter reset, the
- *   prefill kernel, then the decode kernel launched as a programmatic
- *   dependent of the prefill kernel, so decode CTAs start on the room the
- *   prefill grid leaves instead of waiting for it to finish. Block sizes:
- *   >= 16 when there are chunks.
+ *   Everything is enqueued on `stream`: the prefill kernel, then the decode
+ *   kernel launched as a programmatic dependent of the prefill kernel, so
+ *   decode CTAs start on the room the prefill grid leaves instead of
+ *   waiting for it to finish (the workspace's split-KV counters reset
+ *   themselves, as for paged_attn_decode). Block sizes: >= 16 when there
+ *   are chunks.
  */
 pkv_status paged_attn_varlen(void* out, const void* q, pkv_dtype q_dtype,
                              const void* k_cache, const void* v_cache,
