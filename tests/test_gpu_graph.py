@@ -1,7 +1,8 @@
 """CUDA-graph capture of a whole step. A decode step (cache write + decode
-attention, with its split-KV counter reset) and a mixed step (cache write,
-then prefill on a second stream beside decode) are captured once and
-replayed with new inputs copied into the captured buffers. Each replay must
+attention, whose split-KV counters reset themselves) and a mixed step (cache
+write, then one varlen call, or prefill on a second stream beside decode)
+are captured once and replayed with new inputs copied into the captured
+buffers. Each replay must
 equal an eager run on the same inputs bit for bit, and a sample of the
 replayed output must match the oracle."""
 import numpy as np
