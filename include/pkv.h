@@ -325,6 +325,16 @@ pkv_status pkv_get_device_error(void* stream, unsigned int* bits);
 /* Static, human-readable name of a status. */
 const char* pkv_status_string(pkv_status status);
 
+/*
+ * pkv_selftest_bounded_wait — checks the failure path every kernel's waits
+ * share: enqueues on `stream` one CTA whose thread waits on a shared-memory
+ * mbarrier that nothing ever arrives at, with the library's bounded wait
+ * limited to `polls` polls (1 .. 2^20). The wait gives up, sets
+ * PKV_DEVERR_TIMEOUT in the device error word and the kernel returns; the
+ * context stays usable. PKV_ERR_INVALID_ARG for polls outside the range.
+ */
+pkv_status pkv_selftest_bounded_wait(unsigned int polls, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

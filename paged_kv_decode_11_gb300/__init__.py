@@ -6,10 +6,10 @@ ctypes binding (_binding.py) whose functions carry the ABI's names.
 """
 from ._binding import (PkvError, load, paged_attn_decode, paged_attn_decode_noalloc,
                        paged_attn_decode_workspace_size, paged_attn_prefill_chunk, paged_attn_varlen,
-                       pkv_get_device_error, pkv_status_string, reshape_and_cache,
-                       rope_reshape_and_cache)
+                       pkv_get_device_error, pkv_selftest_bounded_wait, pkv_status_string,
+                       reshape_and_cache, rope_reshape_and_cache)
 
 __all__ = ["PkvError", "load", "paged_attn_decode", "paged_attn_decode_noalloc",
            "paged_attn_decode_workspace_size", "paged_attn_prefill_chunk", "paged_attn_varlen",
-           "pkv_get_device_error",
+           "pkv_get_device_error", "pkv_selftest_bounded_wait",
            "pkv_status_string", "reshape_and_cache", "rope_reshape_and_cache"]

@@ -25,7 +25,8 @@ DEVERR_BITS = {0x1: "block id", 0x2: "slot", 0x4: "seq_len", 0x8: "timeout", 0x1
 # Every symbol include/pkv.h declares.
 EXPORTS = ("paged_attn_decode_workspace_size", "paged_attn_decode", "paged_attn_decode_noalloc",
            "paged_attn_prefill_chunk", "paged_attn_varlen", "reshape_and_cache",
-           "rope_reshape_and_cache", "pkv_get_device_error", "pkv_status_string")
+           "rope_reshape_and_cache", "pkv_get_device_error", "pkv_status_string",
+           "pkv_selftest_bounded_wait")
 
 _lib = None
 
@@ -72,6 +73,8 @@ def load(path: str = LIB_PATH):
     L.pkv_get_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint)]
     L.pkv_status_string.restype = ctypes.c_char_p
     L.pkv_status_string.argtypes = [I]
+    L.pkv_selftest_bounded_wait.restype = I
+    L.pkv_selftest_bounded_wait.argtypes = [ctypes.c_uint, P]
     _lib = L
     return L
 
@@ -273,3 +276,10 @@ def pkv_get_device_error(stream=None) -> int:
 
 def pkv_status_string(status: int) -> str:
     return load().pkv_status_string(int(status)).decode()
+
+
+def pkv_selftest_bounded_wait(polls: int, stream=None) -> None:
+    """Enqueue the bounded-wait self-test (a wait that nothing satisfies gives
+    up after `polls` polls and sets the timeout bit of the device error word)."""
+    _check("pkv_selftest_bounded_wait",
+           load().pkv_selftest_bounded_wait(int(polls), _stream(stream)))

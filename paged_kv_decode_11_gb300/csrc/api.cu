@@ -14,6 +14,7 @@
 #include "../../include/pkv.h"
 #pragma GCC visibility pop
 #include "launch.h"
+#include "ptx.cuh"
 
 namespace pkv {
 
@@ -163,6 +164,22 @@ bool valid_dtypes(pkv_dtype q, pkv_dtype kv) {
 }
 
 }  // namespace
+
+// One thread waits on an mbarrier with no arrivals, through the same bounded
+// wait the kernels use; when it gives up it records a timeout and returns.
+__global__ void selftest_wait_kernel(unsigned int polls, unsigned int* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  if (!mbar_wait_bounded(&bar, 0, polls)) atomicOr(err, PKV_DEVERR_TIMEOUT);
+}
+
+pkv_status launch_selftest_wait(unsigned int polls, unsigned int* err, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(polls, err);
+  return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 }  // namespace pkv
 
 using namespace pkv;
@@ -537,6 +554,13 @@ pkv_status rope_reshape_and_cache(void* query, const void* key, const void* valu
   p.num_blocks = num_blocks;
   p.bs_log2 = bs_log2;
   return launch_rope_cache(p, src_dtype, kv_dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_selftest_bounded_wait(unsigned int polls, void* stream) {
+  if (polls < 1 || polls > (1u << 20)) return PKV_ERR_INVALID_ARG;
+  unsigned int* err = err_word();
+  if (err == nullptr) return PKV_ERR_CUDA;
+  return launch_selftest_wait(polls, err, reinterpret_cast<cudaStream_t>(stream));
 }
 
 pkv_status pkv_get_device_error(void* stream, unsigned int* bits) {

@@ -161,3 +161,8 @@ def _rope(lib, **kw):
 ])
 def test_rope_cache_argument_checks(lib, kw, want):
     assert _rope(lib, **kw) == want
+
+
+@pytest.mark.parametrize("polls", [0, (1 << 20) + 1])
+def test_selftest_wait_argument_check(lib, polls):
+    assert lib.pkv_selftest_bounded_wait(polls, None) == INVALID

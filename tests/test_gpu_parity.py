@@ -378,3 +378,20 @@ def test_mixed_step_vs_oracle():
     assert_close(step.prefill_out, pw, tol(c), "mixed prefill")
     # the step wrote the same cache bytes as the oracle
     assert torch.equal(kc.cpu().view(torch.uint8), ko.view(torch.uint8))
+
+
+# ---- failure path of the bounded waits ---------------------------------------------------
+
+@pytest.mark.parametrize("polls", [1, 64, 4096])
+def test_bounded_wait_gives_up_reports_timeout_and_leaves_the_context_usable(polls):
+    P.pkv_get_device_error()                           # start clear
+    P.pkv_selftest_bounded_wait(polls)
+    assert P.pkv_get_device_error() == 0x8             # PKV_DEVERR_TIMEOUT, nothing else
+    # the next real call runs normally on the same context
+    c = make_case("tiny", 0)
+    kc, vc = product_cache(c)
+    out, lse = run_decode(c, kc, vc)
+    check_device_ok()
+    ko, vo = oracle_cache(c)
+    want, _ = oracle_decode(c, ko, vo)
+    assert_close(out, want, tol(c), "decode after a timed-out wait")
