@@ -62,6 +62,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work budget of the oracle baseline sample")
+    ap.add_argument("--cpu-threads", type=int, default=0,
+                    help="host threads for the oracle legs (0: all cores)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time the workload's prefill chunk alone (paged_attn_prefill_chunk); "
                          "prints a TFLOP/s line instead of the step line")
@@ -270,12 +272,12 @@ def oracle_unit(case, kc, vc, unit, q_cpu):
     return int(case.seq_lens[b]) * case.D * 2 * case.kv_elem_bytes
 
 
-def cpu_baseline(case, seconds: float, seed: int):
+def cpu_baseline(case, seconds: float, seed: int, threads: int = 0):
     """The oracle as it stands, on a bounded sample of (sequence, KV head)
     units of this workload, on the host cores; KV-read GB/s."""
     from oracle import oracle as O
     O.build()
-    O.set_threads(0)
+    O.set_threads(threads)
     rng = np.random.default_rng(seed + 99)
     units = sample_units(case, case.B * case.Hkv, rng)
     q_cpu = case.q.cpu().contiguous()
@@ -388,7 +390,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(case, args.cpu_seconds, args.seed)
+        cpu = cpu_baseline(case, args.cpu_seconds, args.seed, args.cpu_threads)
 
     clocks = ClockSampler.summarise(rows, t0, t1)
     if rank == 0:
@@ -526,7 +528,7 @@ def run_reference(args):
         return
     from oracle import oracle as O
     O.build()
-    O.set_threads(0)
+    O.set_threads(args.cpu_threads)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     case = make_case(args.config, args.seed, device=dev)
     rng = np.random.default_rng(args.seed + 7)
