@@ -41,4 +41,4 @@ def test_bench_uses_oracle_only_in_baseline_legs():
     for m in re.finditer(r"from oracle import oracle", t):
         head = t[:m.start()]
         fn = re.findall(r"\ndef (\w+)\(", head)[-1]
-        assert fn in {"oracle_setup", "oracle_unit", "cpu_baseline", "run_reference"}, fn
+        assert fn in {"oracle_setup", "oracle_units", "cpu_baseline", "run_reference"}, fn
