@@ -272,10 +272,16 @@ def oracle_seconds_per_unit(case, units, q_cpu, threads):
     return max(time.perf_counter() - t, 1e-4) / len(c)
 
 
+ORACLE_THREADS = 0          # host threads of the oracle legs (0: all cores)
+
+
 def oracle_units(case, kc, vc, units, q_cpu):
     """Several (sequence, KV head) units in one oracle call per KV head, so the
     oracle's OpenMP loop over (sequence, query head) has work for every core."""
     from oracle import oracle as O
+    # set before every call: torch's own OpenMP set-up can run in between and,
+    # when both share one OpenMP runtime, reset the thread count
+    O.set_threads(ORACLE_THREADS)
     G = case.G
     nbytes = 0
     for h in sorted({h for _, h in units}):
@@ -290,7 +296,9 @@ def cpu_baseline(case, seconds: float, seed: int, threads: int = 0):
     """The oracle as it stands, on a bounded sample of (sequence, KV head)
     units of this workload, on the host cores; KV-read GB/s."""
     from oracle import oracle as O
+    global ORACLE_THREADS
     O.build()
+    ORACLE_THREADS = threads
     O.set_threads(threads)
     rng = np.random.default_rng(seed + 99)
     units = sample_units(case, case.B * case.Hkv, rng)
@@ -537,7 +545,9 @@ def run_reference(args):
     if rank != 0:
         return
     from oracle import oracle as O
+    global ORACLE_THREADS
     O.build()
+    ORACLE_THREADS = args.cpu_threads
     O.set_threads(args.cpu_threads)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     case = make_case(args.config, args.seed, device=dev)
