@@ -39,3 +39,12 @@ def test_prefill_only_flag_parses(monkeypatch):
     monkeypatch.setattr(sys, "argv", ["bench.py", "--config", "mixed", "--prefill-only"])
     args = bench.parse_args()
     assert args.prefill_only and args.config == "mixed"
+
+
+def test_cpu_baseline_leg_runs_the_oracle_on_a_bounded_sample():
+    import bench
+    c = make_case("tiny", 0, device="cpu")
+    r = bench.cpu_baseline(c, 1.0, 0, 2)
+    assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["value"] > 0
+    assert r["cores"] == 2
+    assert "units of the same workload" in r["sample"]
