@@ -166,7 +166,9 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype,
  *   stream capture. The array starts zero-filled and each call leaves the
  *   counters it used at zero. Every call on a device shares the one array,
  *   so calls that overlap on the GPU (on different streams, or from
- *   different threads) race: serialise them.
+ *   different threads) race: serialise them. After a race, or a call that
+ *   reported a device error, clear the array with
+ *   paged_attn_decode_noalloc_reset before the next call.
  */
 pkv_status paged_attn_decode_noalloc(void* out, const void* q, pkv_dtype q_dtype,
                                      const void* k_cache, const void* v_cache,
@@ -181,6 +183,24 @@ pkv_status paged_attn_decode_noalloc(void* out, const void* q, pkv_dtype q_dtype
                                      const float* v_scales,
                                      int partition_tokens, float* out_lse,
                                      void* stream);
+
+/*
+ * paged_attn_decode_noalloc_reset — the way back to a clean scratch array for
+ * paged_attn_decode_noalloc. The source pages have no counterpart to this
+ * call either. Its callers cannot clear the library's array themselves, yet
+ * its partition counters must be zero when a call starts; a call that ended
+ * with a device error (PKV_DEVERR_TIMEOUT, for instance), or two calls that
+ * overlapped on the GPU, can leave some set, and every later call on that
+ * device is then flagged with PKV_DEVERR_COUNTER or merges stale partials.
+ * This enqueues on `stream` one cudaMemsetAsync that zero-fills the whole
+ * array of the current device (PKV_NOALLOC_SCRATCH_BYTES; it allocates
+ * nothing). Call it, on the stream the decode calls use, after such an error
+ * and before the next paged_attn_decode_noalloc; it must not overlap a
+ * noalloc call on the GPU. Like the decode call, its first use on a device
+ * looks up the array's address, so make that first call outside any stream
+ * capture. PKV_ERR_CUDA if the lookup or the memset fails.
+ */
+pkv_status paged_attn_decode_noalloc_reset(void* stream);
 
 /*
  * paged_attn_prefill_chunk — causal attention of a chunk of new query

@@ -24,7 +24,7 @@ DEVERR_BITS = {0x1: "block id", 0x2: "slot", 0x4: "seq_len", 0x8: "timeout", 0x1
 
 # Every symbol include/pkv.h declares.
 EXPORTS = ("paged_attn_decode_workspace_size", "paged_attn_decode", "paged_attn_decode_noalloc",
-           "paged_attn_prefill_chunk", "paged_attn_varlen", "reshape_and_cache",
+           "paged_attn_decode_noalloc_reset", "paged_attn_prefill_chunk", "paged_attn_varlen", "reshape_and_cache",
            "rope_reshape_and_cache", "pkv_get_device_error", "pkv_status_string",
            "pkv_selftest_bounded_wait")
 
@@ -58,6 +58,8 @@ def load(path: str = LIB_PATH):
     L.paged_attn_decode_noalloc.restype = I
     L.paged_attn_decode_noalloc.argtypes = [P, P, I, P, P, I, P, P, I, I, I, I, I, I, I, I, F, P,
                                             P, I, P, P]
+    L.paged_attn_decode_noalloc_reset.restype = I
+    L.paged_attn_decode_noalloc_reset.argtypes = [P]
     L.paged_attn_prefill_chunk.restype = I
     L.paged_attn_prefill_chunk.argtypes = [P, P, I, P, P, I, P, P, P, I, I, I, I, I, I, I, I, I,
                                            F, P, P, P, P]
@@ -168,6 +170,14 @@ def paged_attn_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch
         _dev_ptr(v_scales, "v_scales"), int(partition_tokens), _dev_ptr(out_lse, "out_lse"),
         _stream(stream))
     _check("paged_attn_decode_noalloc", st)
+
+
+def paged_attn_decode_noalloc_reset(stream=None) -> None:
+    """Zero-fill the scratch array of paged_attn_decode_noalloc on the current
+    device (one cudaMemsetAsync on `stream`, nothing allocated): the way back
+    after a device error or an overlap left its partition counters set."""
+    _check("paged_attn_decode_noalloc_reset",
+           load().paged_attn_decode_noalloc_reset(_stream(stream)))
 
 
 def paged_attn_prefill_chunk(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,

@@ -124,35 +124,46 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Split-KV plan of a decode call: contexts are cut into partitions of
-// `part` tokens (one CTA each). The automatic size is the smallest power of
-// two from 512 to 2048 tokens that keeps the launch at about 3 waves of
-// resident CTAs when contexts average half the maximum (fewer, larger
-// partitions cost less per CTA and leave fewer partials to merge; enough of
-// them keep every SM busy). Below 512 tokens the per-CTA start and merge
-// cost more than the extra parallelism gives back.
-// Workspace: [done counters B*Hkv u64 | partition outputs B*Hq*max_parts*D
-// fp32 | partition log2-sum-exps B*Hq*max_parts fp32], each region 256-byte
-// aligned.
+// Split-KV plan of a decode call. With blocks of 16 tokens or more the flat
+// warp schedule runs (decode_flat.cuh): an explicit partition size makes
+// partitions of that many tokens the units of work, each written to its own
+// slot; the automatic split cuts the batch's pages into equal runs, one per
+// warp, so a unit's slots are at most one per warp. Blocks of fewer than 16
+// tokens take the per-partition kernel, whose automatic partition is the
+// smallest power of two from 512 to 2048 tokens that keeps the launch at
+// about 3 waves of resident CTAs when contexts average half the maximum
+// (below 512 tokens its per-CTA start and merge cost more than the extra
+// parallelism gives back).
+// Workspace: [range claims 2 u64 | done counters B*Hkv u64 | merge-group
+// counters, one u64 per slot | slot outputs rows*D fp32 | slot log2-sum-exps
+// rows fp32], each region 256-byte aligned, with slots = max(B*Hkv*max_parts,
+// B*Hkv + ranges of a full grid) and rows = G * slots.
 struct DecodePlan {
   int part, max_parts;
-  size_t off_o, off_lse, bytes;
+  size_t off_done, off_done1, off_o, off_lse, bytes;
 };
 
 DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                        int max_seq_len, int partition_tokens, int sms) {
   DecodePlan pl{};
+  if (sms <= 0) sms = 148;
   if (partition_tokens > 0) {
     pl.part = partition_tokens;
   } else {
     const int64_t est = (int64_t)num_seqs * num_kv_heads * std::max(1, max_seq_len / 2);
-    const int64_t target = (int64_t)(sms > 0 ? sms : 148) * kDecodeWorkers * 3;
+    const int64_t target = (int64_t)sms * kDecodeWorkers * 3;
     pl.part = 512;
     while (pl.part < 2048 && est / pl.part > target) pl.part *= 2;
   }
   pl.max_parts = std::max(1, (max_seq_len + pl.part - 1) / pl.part);
-  const size_t rows = (size_t)num_seqs * num_q_heads * pl.max_parts;
-  pl.off_o = align256((size_t)num_seqs * num_kv_heads * 8);
+  const size_t units = (size_t)num_seqs * num_kv_heads;
+  const size_t flat_slots =
+      units + (size_t)sms * kDecodeWorkers * kDecodeWarps * kFlatRangesPerWarp;
+  const size_t slots = std::max(units * (size_t)pl.max_parts, flat_slots);
+  const size_t rows = slots * (size_t)(num_q_heads / num_kv_heads);
+  pl.off_done = 256;
+  pl.off_done1 = pl.off_done + align256(units * 8);
+  pl.off_o = pl.off_done1 + align256(slots * 8);
   pl.off_lse = pl.off_o + align256(rows * head_dim * sizeof(float));
   pl.bytes = pl.off_lse + align256(rows * sizeof(float));
   return pl;
@@ -275,7 +286,9 @@ pkv_status decode_setup(void* out, const void* q, pkv_dtype q_dtype, const void*
   p.k_scales = k_scales;
   p.v_scales = v_scales;
   p.out_lse = out_lse;
-  p.done = reinterpret_cast<unsigned long long*>(ws);
+  p.claims = reinterpret_cast<unsigned long long*>(ws);
+  p.done = reinterpret_cast<unsigned long long*>(ws + pl.off_done);
+  p.done1 = reinterpret_cast<unsigned long long*>(ws + pl.off_done1);
   p.ws_o = reinterpret_cast<float*>(ws + pl.off_o);
   p.ws_lse = reinterpret_cast<float*>(ws + pl.off_lse);
   p.err = err;
@@ -292,6 +305,10 @@ pkv_status decode_setup(void* out, const void* q, pkv_dtype q_dtype, const void*
   p.max_parts = pl.max_parts;
   p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   p.wait_prior = 1;
+  p.explicit_parts = partition_tokens > 0 ? 1 : 0;
+  p.min_atoms = kFlatMinPages;
+  p.cap = (int)std::min<int64_t>(max_seq_len, (int64_t)max_blocks_per_seq << bs_log2);
+  p.ppp = partition_tokens > 0 ? partition_tokens / 16 : 0;     // 16-token pages
   return PKV_OK;
 }
 

@@ -90,6 +90,35 @@ __device__ __forceinline__ void lds_run(uint32_t (&w)[D / 32], uint32_t page, in
   }
 }
 
+// E4M3 caches run f16 MMAs, so a bf16 query is converted to f16 first. To keep
+// that conversion from overflowing (bf16 reaches 2^128, f16 only 65504) or
+// losing the bits of small values, the query is scaled by 2^-e, with e chosen
+// so that the largest magnitude of the scaled rows lies in [2^14, 2^15), and
+// the scores are scaled back by 2^e. Both scalings are by powers of two, so
+// they are exact: every element within 2^-28 of the largest converts to f16
+// exactly, and where the unscaled conversion was exact the scores come out
+// bit for bit the same. `max_abs` holds the bf16 bits (sign cleared) of the
+// largest magnitude.
+__device__ __forceinline__ int q_f16_shift(uint32_t max_abs) {
+  const int eb = (int)((max_abs >> 7) & 0xFFu);     // biased exponent; 0: zero or subnormal
+  const int e = eb == 0 ? -64 : eb - 127 - 14;
+  return min(max(e, -64), 126);
+}
+
+// 2^e as a float, for e in [-126, 127].
+__device__ __forceinline__ float pow2f(int e) { return __int_as_float((127 + e) << 23); }
+
+// Largest bf16 magnitude (bits, sign cleared) of the two halves of a word.
+__device__ __forceinline__ uint32_t bf16x2_max_abs(uint32_t w) {
+  return max(w & 0x7FFFu, (w >> 16) & 0x7FFFu);
+}
+
+// Two bf16 values times 2^-e (exact, a power of two), rounded to f16x2.
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float inv_pow2) {
+  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+  return pack_f16x2(f.x * inv_pow2, f.y * inv_pow2);
+}
+
 // Token (0..15) of S accumulator element e (0, 1) of n-tile j for a thread
 // with c = lane % 4.
 template <int KV>
@@ -109,23 +138,16 @@ __device__ __forceinline__ int o_col_dim(int t, int c, int e) {
 
 // Q fragments (A operand, 16 rows x D) for the page products. rowg / rowg8
 // point at the D values of query rows g and g + 8 (nullptr = padding row, 0).
-// E4M3 caches use f16 MMAs: q is converted to f16 and the contraction index
-// follows the permutation described at the top of this file.
+// E4M3 caches use f16 MMAs: a bf16 q is scaled per row by 2^-sh (q_f16_shift;
+// sh0 for row g, sh8 for row g + 8, 0 otherwise) and converted to f16, and the
+// contraction index follows the permutation described at the top of this file.
 template <int D, int KV, bool QBF16>
 __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[D / 16][4], const void* rowg,
-                                             const void* rowg8, int lane) {
+                                             const void* rowg8, int lane, int& sh0, int& sh8) {
   const int c = lane & 3;
   auto ld2 = [&](const void* row, int d) -> uint32_t {
     if (row == nullptr) return 0u;
-    uint32_t raw = *reinterpret_cast<const uint32_t*>(
-        static_cast<const uint16_t*>(row) + d);
-    if constexpr (KV == KV_E4M3 && QBF16) {
-      __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&raw);
-      float2 f = __bfloat1622float2(v);
-      return pack_f16x2(f.x, f.y);
-    } else {
-      return raw;
-    }
+    return *reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(row) + d);
   };
 #pragma unroll
   for (int s = 0; s < D / 16; ++s) {
@@ -142,6 +164,31 @@ __device__ __forceinline__ void load_q_frags(uint32_t (&qf)[D / 16][4], const vo
     qf[s][1] = ld2(rowg8, d0);
     qf[s][2] = ld2(rowg, d1);
     qf[s][3] = ld2(rowg8, d1);
+  }
+  sh0 = sh8 = 0;
+  if constexpr (KV == KV_E4M3 && QBF16) {
+    // the four lanes of a quad hold the whole of rows g and g + 8
+    uint32_t m0 = 0u, m8 = 0u;
+#pragma unroll
+    for (int s = 0; s < D / 16; ++s) {
+      m0 = max(m0, max(bf16x2_max_abs(qf[s][0]), bf16x2_max_abs(qf[s][2])));
+      m8 = max(m8, max(bf16x2_max_abs(qf[s][1]), bf16x2_max_abs(qf[s][3])));
+    }
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      m0 = max(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+      m8 = max(m8, __shfl_xor_sync(0xffffffffu, m8, o));
+    }
+    sh0 = q_f16_shift(m0);
+    sh8 = q_f16_shift(m8);
+    const float f0 = pow2f(-sh0), f8 = pow2f(-sh8);
+#pragma unroll
+    for (int s = 0; s < D / 16; ++s) {
+      qf[s][0] = bf16x2_to_f16x2_scaled(qf[s][0], f0);
+      qf[s][1] = bf16x2_to_f16x2_scaled(qf[s][1], f8);
+      qf[s][2] = bf16x2_to_f16x2_scaled(qf[s][2], f0);
+      qf[s][3] = bf16x2_to_f16x2_scaled(qf[s][3], f8);
+    }
   }
 }
 

@@ -41,11 +41,12 @@ __device__ __forceinline__ int ot_row_dim(int t, int g, int r8) {
 }
 
 // Q^T fragments (B operand, D x 8NT) from the G query rows [G][D] of a GQA
-// group in shared memory; head columns >= G are zero. 16-bit q, converted to
-// f16 for E4M3 caches.
+// group; head columns >= G are zero. 16-bit q; for E4M3 caches a bf16 q is
+// scaled by 2^-qshift (q_f16_shift over the whole group, so one factor
+// serves every score of the CTA) and converted to f16. qshift is 0 otherwise.
 template <int D, int KV, bool QBF16, int NT>
 __device__ __forceinline__ void load_qT_frags(uint32_t (&qf)[NT][D / 16][2],
-                                              const uint16_t* qs, int G, int lane) {
+                                              const uint16_t* qs, int G, int lane, int& qshift) {
   const int g = lane >> 2, c = lane & 3;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
@@ -62,17 +63,31 @@ __device__ __forceinline__ void load_qT_frags(uint32_t (&qf)[NT][D / 16][2],
         d0 = 16 * s + 2 * c;
         d1 = d0 + 8;
       }
-      uint32_t r0 = *reinterpret_cast<const uint32_t*>(row + d0);
-      uint32_t r1 = *reinterpret_cast<const uint32_t*>(row + d1);
-      if constexpr (KV == KV_E4M3 && QBF16) {
-        float2 f0 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&r0));
-        float2 f1 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&r1));
-        r0 = pack_f16x2(f0.x, f0.y);
-        r1 = pack_f16x2(f1.x, f1.y);
-      }
+      const uint32_t r0 = *reinterpret_cast<const uint32_t*>(row + d0);
+      const uint32_t r1 = *reinterpret_cast<const uint32_t*>(row + d1);
       qf[nt][s][0] = live ? r0 : 0u;
       qf[nt][s][1] = live ? r1 : 0u;
     }
+  }
+  qshift = 0;
+  if constexpr (KV == KV_E4M3 && QBF16) {
+    // the warp holds every element of the group: one shift for all of it
+    uint32_t m = 0u;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int s = 0; s < D / 16; ++s)
+        m = max(m, max(bf16x2_max_abs(qf[nt][s][0]), bf16x2_max_abs(qf[nt][s][1])));
+    m = __reduce_max_sync(0xffffffffu, m);
+    qshift = q_f16_shift(m);
+    const float f = pow2f(-qshift);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int s = 0; s < D / 16; ++s) {
+        qf[nt][s][0] = bf16x2_to_f16x2_scaled(qf[nt][s][0], f);
+        qf[nt][s][1] = bf16x2_to_f16x2_scaled(qf[nt][s][1], f);
+      }
   }
 }
 
@@ -274,6 +289,26 @@ __device__ __forceinline__ void vp_page(float (&oacc)[NT][D / 16][4], const uint
     }
   }
 }
+
+// Zeroes rows [valid, 16) of a page in shared memory (all its boxes). The
+// swizzle only permutes 16-byte chunks inside a row, so a row's bytes are
+// the row's whole 128-byte (or 64-byte) stripe of each box.
+template <int D, int KV>
+__device__ __forceinline__ void zero_page_rows(uint8_t* page, int valid, int lane) {
+  using Geo = PageGeom<D, KV>;
+  constexpr int CPR = Geo::ROW_BYTES / 16;
+  for (int i = lane; i < (kBS - valid) * CPR; i += 32) {
+    const int r = valid + i / CPR, x = (i % CPR) * 16;
+    *reinterpret_cast<uint4*>(page + (x / Geo::BOX_ROW_BYTES) * Geo::BOX_BYTES +
+                              r * Geo::BOX_ROW_BYTES + x % Geo::BOX_ROW_BYTES) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// The decode kernels' softmax keeps, per column, a reference max that moves
+// only when a page's max exceeds it by more than this (log2 units), so the
+// accumulators are rescaled rarely; the probabilities stay below 2^8.
+constexpr float kRefSlackLog2 = 8.f;
 
 // Max / sum over the 8 lanes that share c = lane % 4 (the 8 token rows g).
 __device__ __forceinline__ float col_max8(float v) {

@@ -41,21 +41,6 @@ struct DecodeCfg {
       1024 + (RING_BYTES > OBUF_BYTES ? RING_BYTES : OBUF_BYTES);
 };
 
-// Zeroes rows [valid, 16) of a page in shared memory (all its boxes). The
-// swizzle only permutes 16-byte chunks inside a row, so a row's bytes are
-// the row's whole 128-byte (or 64-byte) stripe of each box.
-template <int D, int KV>
-__device__ __forceinline__ void zero_page_rows(uint8_t* page, int valid, int lane) {
-  using Geo = PageGeom<D, KV>;
-  constexpr int CPR = Geo::ROW_BYTES / 16;
-  for (int i = lane; i < (kBS - valid) * CPR; i += 32) {
-    const int r = valid + i / CPR, x = (i % CPR) * 16;
-    *reinterpret_cast<uint4*>(page + (x / Geo::BOX_ROW_BYTES) * Geo::BOX_BYTES +
-                              r * Geo::BOX_ROW_BYTES + x % Geo::BOX_ROW_BYTES) =
-        make_uint4(0u, 0u, 0u, 0u);
-  }
-}
-
 template <int D, int KV, bool QBF16, int NT, int NW, int NST, bool GATHER>
 __global__ void __launch_bounds__(NW * 32)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -189,7 +174,8 @@ __global__ void __launch_bounds__(NW * 32)
   // ---- query fragments (heads in N), straight from global memory --------------------
   const uint16_t* qb = static_cast<const uint16_t*>(p.q) + ((int64_t)b * p.Hq + h * G) * D;
   uint32_t qf[NT][D / 16][2];
-  load_qT_frags<D, KV, QBF16, NT>(qf, qb, G, lane);
+  int qshift;
+  load_qT_frags<D, KV, QBF16, NT>(qf, qb, G, lane, qshift);
 
   float oacc[NT][D / 16][4];
 #pragma unroll
@@ -203,7 +189,8 @@ __global__ void __launch_bounds__(NW * 32)
     m[nt][0] = m[nt][1] = -INFINITY;
     l[nt][0] = l[nt][1] = 0.f;
   }
-  const float sl2 = p.qk_scale_log2 * (KV == KV_E4M3 ? p.k_scales[h] : 1.f);
+  // q was scaled by 2^-qshift for the f16 MMAs: scale the scores back (exact)
+  const float sl2 = p.qk_scale_log2 * (KV == KV_E4M3 ? p.k_scales[h] : 1.f) * pow2f(qshift);
   const int tk0 = st_row_token<KV>(g, 0), tk8 = st_row_token<KV>(g, 1);
 
   for (int k = 0; k < nmine; ++k) {
@@ -245,27 +232,47 @@ __global__ void __launch_bounds__(NW * 32)
       kq_page<D, KV, NT>(s, qf, kpage, lane);
     }
 
+    // online softmax in the log2 domain, against a reference max per column
+    // that moves only when the page's max outgrows it by kRefSlackLog2, so the
+    // accumulators are rescaled rarely (the probabilities stay below 2^8)
     const bool v0 = tbase + tk0 < tok1, v8 = tbase + tk8 < tok1;
+    float pmax[NT][2];
+    bool move = false;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const float x0 = v0 ? s[nt][e] * sl2 : -INFINITY;
-        const float x8 = v8 ? s[nt][2 + e] * sl2 : -INFINITY;
-        const float mx = col_max8(fmaxf(x0, x8));
-        const float mn = fmaxf(m[nt][e], mx);
-        const float ms = (mn == -INFINITY) ? 0.f : mn;
-        const float alpha = exp2f(m[nt][e] - ms);
-        m[nt][e] = mn;
-        const float p0 = exp2f(x0 - ms), p8 = exp2f(x8 - ms);
-        l[nt][e] = l[nt][e] * alpha + p0 + p8;
+        s[nt][e] = v0 ? s[nt][e] * sl2 : -INFINITY;
+        s[nt][2 + e] = v8 ? s[nt][2 + e] * sl2 : -INFINITY;
+        pmax[nt][e] = col_max8(fmaxf(s[nt][e], s[nt][2 + e]));
+        move |= pmax[nt][e] > m[nt][e] + kRefSlackLog2;
+      }
+    if (__any_sync(0xffffffffu, move)) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          if (pmax[nt][e] > m[nt][e] + kRefSlackLog2) {
+            const float alpha = m[nt][e] == -INFINITY ? 0.f : exp2f(m[nt][e] - pmax[nt][e]);
+            m[nt][e] = pmax[nt][e];
+            l[nt][e] *= alpha;
+#pragma unroll
+            for (int t = 0; t < D / 16; ++t) {
+              oacc[nt][t][e] *= alpha;
+              oacc[nt][t][2 + e] *= alpha;
+            }
+          }
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float ms = m[nt][e] == -INFINITY ? 0.f : m[nt][e];
+        const float p0 = exp2f(s[nt][e] - ms), p8 = exp2f(s[nt][2 + e] - ms);
+        l[nt][e] += p0 + p8;
         s[nt][e] = p0;
         s[nt][2 + e] = p8;
-#pragma unroll
-        for (int t = 0; t < D / 16; ++t) {
-          oacc[nt][t][e] *= alpha;
-          oacc[nt][t][2 + e] *= alpha;
-        }
       }
     uint32_t pb[NT][2];
     pT_frags<KV, NT>(pb, s);

@@ -67,3 +67,13 @@ extern "C" pkv_status paged_attn_decode_noalloc(
                            partition_tokens, out_lse, scratch, (size_t)PKV_NOALLOC_SCRATCH_BYTES,
                            stream);
 }
+
+extern "C" pkv_status paged_attn_decode_noalloc_reset(void* stream) {
+  void* scratch = scratch_address();
+  if (scratch == nullptr) return PKV_ERR_CUDA;
+  // a memset of the array in place: nothing is allocated
+  return cudaMemsetAsync(scratch, 0, (size_t)PKV_NOALLOC_SCRATCH_BYTES,
+                         reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}

@@ -139,7 +139,8 @@ __global__ void __launch_bounds__((kPrefillConsumers + 1) * 32)
   const void* rowg = v0 ? qbase + ((int64_t)(q0 + qi0) * p.Hq + hq0) * D : nullptr;
   const void* rowg8 = v8 ? qbase + ((int64_t)(q0 + qi8) * p.Hq + hq8) * D : nullptr;
   uint32_t qf[D / 16][4];
-  load_q_frags<D, KV, QBF16>(qf, rowg, rowg8, lane);
+  int qsh0, qsh8;
+  load_q_frags<D, KV, QBF16>(qf, rowg, rowg8, lane, qsh0, qsh8);
   // last key each row may see (-1: none)
   const int lim0 = v0 ? P + qi0 : -1;
   const int lim8 = v8 ? P + qi8 : -1;
@@ -149,7 +150,10 @@ __global__ void __launch_bounds__((kPrefillConsumers + 1) * 32)
 #pragma unroll
   for (int t = 0; t < D / 8; ++t) oacc[t][0] = oacc[t][1] = oacc[t][2] = oacc[t][3] = 0.f;
   float m0 = -INFINITY, m8 = -INFINITY, l0 = 0.f, l8 = 0.f;
+  // rows g and g + 8 of q were scaled by 2^-qsh for the f16 MMAs: scale their
+  // scores back (exact)
   const float sl2 = p.qk_scale_log2 * (KV == KV_E4M3 ? p.k_scales[h] : 1.f);
+  const float sl2_0 = sl2 * pow2f(qsh0), sl2_8 = sl2 * pow2f(qsh8);
 
   for (int t = 0; t < n_tiles; ++t) {
     const int st = t % NST;
@@ -182,8 +186,8 @@ __global__ void __launch_bounds__((kPrefillConsumers + 1) * 32)
           for (int e = 0; e < 2; ++e) {
             const int j = 2 * pg + jj;
             const int key = kbase + pg * kBS + s_col_token<KV>(jj, c, e);
-            s[j][e] = key <= lim0 ? s[j][e] * sl2 : -INFINITY;
-            s[j][2 + e] = key <= lim8 ? s[j][2 + e] * sl2 : -INFINITY;
+            s[j][e] = key <= lim0 ? s[j][e] * sl2_0 : -INFINITY;
+            s[j][2 + e] = key <= lim8 ? s[j][2 + e] * sl2_8 : -INFINITY;
             mx0 = fmaxf(mx0, s[j][e]);
             mx8 = fmaxf(mx8, s[j][2 + e]);
           }

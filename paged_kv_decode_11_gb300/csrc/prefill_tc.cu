@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
   __shared__ uint64_t s_bar[NG][2], o_bar[NG][2], p_bar[NG][2];
   __shared__ uint64_t ready_bar, recv_bar;              // cluster hand-off (SPLIT == 2)
   __shared__ uint32_t tmem_base;
+  __shared__ float s_qpow[kTcRows];                     // KV8, bf16 q: 2^shift of each row
 
   // a decode launched behind this kernel as a programmatic dependent may take
   // the SM room this grid leaves as soon as all of its CTAs are running
@@ -367,19 +368,31 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
     const uint16_t* src =
         static_cast<const uint16_t*>(p.q) + ((int64_t)(q0 + (rvalid ? qi : 0)) * p.Hq +
                                              (rvalid ? hq : 0)) * D;
+    // the MMAs run in f16 against an E4M3 cache: a bf16 query row is scaled by
+    // 2^-shift (q_f16_shift of the row) and rounded to f16; its scores are
+    // scaled back by 2^shift in the softmax
+    float qinv = 1.f;
+    if constexpr (KV8 && QBF16) {
+      uint32_t mx = 0u;
+      if (rvalid) {
+#pragma unroll 4
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src + 8 * c);
+          mx = max(mx, max(max(bf16x2_max_abs(v.x), bf16x2_max_abs(v.y)),
+                           max(bf16x2_max_abs(v.z), bf16x2_max_abs(v.w))));
+        }
+      }
+      const int sh = rvalid ? q_f16_shift(mx) : 0;
+      qinv = pow2f(-sh);
+      s_qpow[r] = pow2f(sh);
+    }
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
       uint4 v = rvalid ? *reinterpret_cast<const uint4*>(src + 8 * c)
                        : make_uint4(0u, 0u, 0u, 0u);
       if constexpr (KV8 && QBF16) {
-        // the MMAs run in f16 against an E4M3 cache: round the bf16 query to f16
-        uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
-          w[k] = pack_f16x2(f.x, f.y);
-        }
-        v = make_uint4(w[0], w[1], w[2], w[3]);
+        v = make_uint4(bf16x2_to_f16x2_scaled(v.x, qinv), bf16x2_to_f16x2_scaled(v.y, qinv),
+                       bf16x2_to_f16x2_scaled(v.z, qinv), bf16x2_to_f16x2_scaled(v.w, qinv));
       }
       *reinterpret_cast<uint4*>(pQ + (c / 8) * Cfg::Q_BOX + swz128(r, c % 8)) = v;
     }
@@ -476,7 +489,8 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
   // ---- warps 0 .. 4 NG - 1: the softmax groups, one row per thread each ------------
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   const int lim = rvalid ? P0 + qi : -1;                // last key this row sees
-  const float sl2 = p.qk_scale_log2 * (KV8 ? p.k_scales[h] : 1.f);
+  const float sl2 = p.qk_scale_log2 * (KV8 ? p.k_scales[h] : 1.f) *
+                   ((KV8 && QBF16) ? s_qpow[r] : 1.f);     // undoes the row's q scaling
   const uint32_t tOg = tO + grp * D;
   const int n_mine = (n_tiles - grp + NG - 1) / NG;     // this group's tiles
   float m_ref = -INFINITY, l = 0.f;

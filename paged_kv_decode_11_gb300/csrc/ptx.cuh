@@ -117,6 +117,18 @@ __device__ __forceinline__ void cp_async16_hint(void* smem_dst, const void* gsrc
                : "memory");
 }
 
+// 4-byte asynchronous global -> shared copy (through L1); completes by
+// cp_async_wait_all.
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gsrc)
+               : "memory");
+}
+
+// Waits until every cp.async this thread issued has landed.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // The mbarrier receives one arrival once every cp.async this thread issued so
 // far has landed (the arrival counts toward the barrier's expected count).
 __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
