@@ -26,8 +26,11 @@
  * Conventions shared by every entry point
  *  - All pointers are DEVICE pointers unless stated; the caller owns every
  *    buffer. The library allocates no device memory and keeps no per-call
- *    state; the only library-wide state is one device error word and a
- *    cached per-device SM count.
+ *    state. Its library-wide state: per device, the device error word, the
+ *    scratch array of paged_attn_decode_noalloc (PKV_NOALLOC_SCRATCH_BYTES,
+ *    a file-scope device array held by every GPU that loads the library),
+ *    the cached SM count and the one-time kernel attribute and grid-size
+ *    settings; process-wide, the driver's tensor-map encoder entry point.
  *  - `stream` is a cudaStream_t passed as an opaque pointer (NULL = the
  *    legacy default stream). Work is only enqueued; nothing synchronises,
  *    except pkv_get_device_error.

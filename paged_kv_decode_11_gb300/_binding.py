@@ -128,8 +128,9 @@ def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
                       out_lse: Optional[torch.Tensor] = None,
                       workspace: Optional[torch.Tensor] = None, stream=None) -> None:
     """out[B, Hq, D] <- decode attention of q[B, Hq, D] over the paged cache
-    k_cache/v_cache[num_blocks, Hkv, BS, D]. A zero-filled workspace tensor
-    is allocated with torch when none is given (reuse one across calls)."""
+    k_cache/v_cache[num_blocks, Hkv, BS, D]. Without a workspace tensor, a
+    zero-filled one is allocated with torch on every call (an allocation and a
+    fill kernel per call): pass one and reuse it across calls."""
     B, Hq, D = q.shape
     nb, hkv, bs, d2 = k_cache.shape
     assert d2 == D and out.shape == q.shape and out.dtype == q.dtype
@@ -210,7 +211,9 @@ def paged_attn_varlen(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
                       workspace: Optional[torch.Tensor] = None, stream=None) -> None:
     """out[T, Hq, D] <- attention of a whole step: q rows 0..num_decode_seqs-1
     are the decode sequences, the rest the prefill chunks that
-    query_start_loc [num_seqs + 1] delimits. One call, one stream."""
+    query_start_loc [num_seqs + 1] delimits. One call, one stream. Without a
+    workspace tensor, a zero-filled one is allocated with torch on every call
+    (an allocation and a fill kernel per call): pass one and reuse it."""
     T, Hq, D = q.shape
     nb, hkv, bs, _ = k_cache.shape
     n = seq_lens.shape[0]

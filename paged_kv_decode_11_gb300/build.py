@@ -50,16 +50,16 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False,
-          out: str = LIB, defines=()) -> str:
-    """Compile and link libpkv; `out` and `defines` (-D flags) build tuning
-    variants of the same sources elsewhere."""
-    if not force and out == LIB and up_to_date():
+def build(force: bool = False, verbose: bool = False, ptxas_v: bool = False) -> str:
+    """Compile and link libpkv (only when a source is newer than the library,
+    unless force); ptxas_v prints the registers and spills of every kernel."""
+    out = LIB
+    if not force and up_to_date():
         return out
-    obj_dir = OBJ_DIR if out == LIB else out + ".objs"
+    obj_dir = OBJ_DIR
     os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
-    extra = (["-Xptxas", "-v"] if ptxas_v else []) + [f"-D{d}" for d in defines]
+    extra = ["-Xptxas", "-v"] if ptxas_v else []
 
     def compile_one(src):
         obj = os.path.join(obj_dir, os.path.basename(src) + ".o")

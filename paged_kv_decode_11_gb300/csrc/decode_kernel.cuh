@@ -57,6 +57,7 @@ __global__ void __launch_bounds__(NW * 32)
   __shared__ float red_l[NW][NH];
   __shared__ int s_ids[NIDS];
   __shared__ int s_last;
+  __shared__ int s_stuck;         // a warp's copies may still land in the ring
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
@@ -120,6 +121,7 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
       for (int s = 0; s < NST; ++s) mbar_init(&bars[w][s], GATHER ? 32 : 1);
     fence_barrier_init();
+    s_stuck = 0;
   }
   __syncthreads();
 
@@ -199,9 +201,13 @@ __global__ void __launch_bounds__(NW * 32)
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) {
       if (lane == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
-      // let what this warp still has in flight land (bounded), then stop
+      // let what this warp still has in flight land (bounded), then stop; if
+      // that wait gives up too, a late copy could still land in the ring, so
+      // the CTA leaves the ring's space (the merge buffer below) alone
+      bool drained = true;
       for (int kk = k + 1; kk < issued; ++kk)
-        mbar_wait_bounded(&bars[warp][kk % NST], (kk / NST) & 1, 1u << 16);
+        drained &= mbar_wait_bounded(&bars[warp][kk % NST], (kk / NST) & 1, 1u << 16);
+      if (!__all_sync(0xffffffffu, drained) && lane == 0) s_stuck = 1;
       break;
     }
     const uint32_t kpage = wbase + st * STAGE;
@@ -301,6 +307,16 @@ __global__ void __launch_bounds__(NW * 32)
       }
     }
   __syncthreads();  // every warp is done with its ring: the ring's space is free
+  if (s_stuck) {
+    // (after a timeout whose drain gave up; the error word holds the timeout)
+    // no output or partial from this CTA, only its count, so that the
+    // (b, h) counter still completes and comes back to zero
+    if (nparts > 1 && tid == 0) {
+      unsigned long long* ctr = p.done + (int64_t)b * p.Hkv + h;
+      if (atom_add_acq_rel_gpu(ctr, 1ull) + 1 == (unsigned long long)nparts) *ctr = 0ull;
+    }
+    return;
+  }
   float* obuf = reinterpret_cast<float*>(basep);   // [NW][G][D]
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
