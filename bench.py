@@ -21,7 +21,6 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -64,6 +63,12 @@ def parse_args():
                     help="CPU work budget of the oracle baseline sample")
     ap.add_argument("--cpu-threads", type=int, default=0,
                     help="host threads for the oracle legs (0: all cores)")
+    ap.add_argument("--record-traffic", metavar="NCU_CSV", default=None,
+                    help="store the DRAM bytes of the last decode launch in this ncu --csv "
+                         "capture (dram__bytes_read.sum, dram__bytes_write.sum) as the "
+                         "workload's traffic, keyed by the current decode source hash")
+    ap.add_argument("--capture-command", default="",
+                    help="with --record-traffic: the command the capture ran, kept with it")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time the workload's prefill chunk alone (paged_attn_prefill_chunk); "
                          "prints a TFLOP/s line instead of the step line")
@@ -171,10 +176,11 @@ class ClockSampler:
 
 # ---- profile-derived traffic ----------------------------------------------------
 
-# The sources the decode kernel and its launch plan are built from: a traffic
-# figure taken by ncu stays valid while none of them changes.
-DECODE_SOURCES = ("api.cu", "common.cuh", "decode.cu", "decode_frags.cuh", "decode_kernel.cuh",
-                  "launch.h", "ptx.cuh")
+# The device code the decode kernels are built from and their partition
+# planner: a traffic figure ncu took stays valid while none of these changes.
+DECODE_SOURCES = ("common.cuh", "decode.cu", "decode_flat.cuh", "decode_frags.cuh",
+                  "decode_kernel.cuh", "launch.h", "plan.h", "ptx.cuh")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
 
 
 def source_hash() -> str:
@@ -188,17 +194,64 @@ def source_hash() -> str:
 
 
 def profile_traffic(config: str):
-    """DRAM bytes per decode-attention call from the committed ncu summary of
-    this workload, if it was taken on the current kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"decode_attention.{config}.md")
-    if not os.path.exists(path):
+    """DRAM bytes per decode call of this workload, as ncu measured them
+    (profiles/decode_traffic.json, written by profiles/decode_traffic.py),
+    if they were taken on the current decode sources; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f).get(config)
+    except (OSError, ValueError):
         return None
-    txt = open(path).read()
-    mh = re.search(r"source_hash:\s*([0-9a-f]+)", txt)
-    mt = re.search(r"dram_bytes_per_call:\s*([0-9]+)", txt)
-    if not mh or not mt or mh.group(1) != source_hash():
+    if not rec or rec.get("source_hash") != source_hash():
         return None
-    return int(mt.group(1))
+    return int(rec["dram_bytes_per_call"])
+
+
+_BYTE_UNITS = {"byte": 1, "kbyte": 1e3, "mbyte": 1e6, "gbyte": 1e9, "tbyte": 1e12}
+
+
+def record_traffic(args):
+    """Reads an ncu --csv capture of this workload's bench run and stores the
+    DRAM bytes (read + write) of its last decode launch in the traffic file."""
+    import csv
+    launches = {}
+    with open(args.record_traffic, newline="") as f:
+        rows = [r for r in csv.reader(f) if r]
+    hdr_i = next(i for i, r in enumerate(rows) if "Metric Name" in r)
+    hdr = rows[hdr_i]
+    col = {name: hdr.index(name) for name in ("ID", "Kernel Name", "Metric Name", "Metric Unit",
+                                              "Metric Value")}
+    for r in rows[hdr_i + 1:]:
+        if len(r) < len(hdr):
+            continue
+        name = r[col["Kernel Name"]]
+        if "decode_kernel" not in name and "decode_flat_kernel" not in name:
+            continue
+        metric = r[col["Metric Name"]]
+        if metric not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+            continue
+        unit = _BYTE_UNITS[r[col["Metric Unit"]].lower()]
+        val = float(r[col["Metric Value"]].replace(",", "")) * unit
+        launches.setdefault(int(r[col["ID"]]), {})[metric] = val
+    last = max(i for i, m in launches.items() if len(m) == 2)
+    m = launches[last]
+    try:
+        with open(TRAFFIC_FILE) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        data = {}
+    data[args.config] = {
+        "source_hash": source_hash(),
+        "dram_bytes_per_call": int(round(m["dram__bytes_read.sum"] + m["dram__bytes_write.sum"])),
+        "dram_bytes_read": int(round(m["dram__bytes_read.sum"])),
+        "dram_bytes_write": int(round(m["dram__bytes_write.sum"])),
+        "launch_id": last,
+        "command": args.capture_command,
+    }
+    with open(TRAFFIC_FILE, "w") as f:
+        json.dump(data, f, indent=1, sort_keys=True)
+        f.write("\n")
+    print(json.dumps({args.config: data[args.config]}))
 
 
 def measured_hbm_peak():
@@ -360,29 +413,35 @@ def run_ours(args):
     if rank == 0:
         sampler.start()
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
     barrier(world)
     torch.cuda.synchronize()
     t0 = time.time()
     for i in range(K):
         flush.fill_(i & 0xFF)                       # evict the previous step from L2
-        e0, ea, e1 = ev[i]
-        e0.record(stream)
-        if isinstance(step, MixedStep):
-            one_step()
-            ea.record(stream)                       # unused for the mixed step
-        else:
-            step.write_cache(stream)
-            ea.record(stream)
-            step.attend(stream)
-        e1.record(stream)
+        ev[i][0].record(stream)
+        one_step()                                  # the step's own call(s)
+        ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     t1 = time.time()
+    # the decode kernel alone, for its roofline: the cache write, then an event,
+    # then the attention call (which then cannot start before the write ends)
+    attn_ms = None
+    if not isinstance(step, MixedStep):
+        ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            step.write_cache(stream)
+            ev2[i][0].record(stream)
+            step.attend(stream)
+            ev2[i][1].record(stream)
+        torch.cuda.synchronize()
+        attn_ms = [a.elapsed_time(b) for a, b in ev2]
     rows = sampler.stop() if rank == 0 else []
-    step_ms = [a.elapsed_time(c) for a, _, c in ev]
-    attn_ms = [b.elapsed_time(c) for _, b, c in ev] if not isinstance(step, MixedStep) else None
+    step_ms = [a.elapsed_time(b) for a, b in ev]
     ms_local = float(np.mean(step_ms))
     ms = allreduce(ms_local, "max", world)
     total_bytes = allreduce(float(kv_bytes), "sum", world)
@@ -706,7 +765,9 @@ def run_prefill_only(args):
 
 def main():
     args = parse_args()
-    if args.impl == "reference":
+    if args.record_traffic:
+        record_traffic(args)
+    elif args.impl == "reference":
         run_reference(args)
     elif args.prefill_only:
         run_prefill_only(args)

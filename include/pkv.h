@@ -147,6 +147,33 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype,
                              void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/*
+ * paged_attn_decode_step — one decode step of attention: the cache write of
+ * every sequence's new token, then decode attention, in one call ("RoPE + KV
+ * cache write" followed by "Flash Attention Decode", rvLLM: High-performance
+ * LLM inference in Rust, Kernel Compiler Stack, decode step).
+ *   key, value: [num_seqs, Hkv, D] in the q dtype, the new token of each
+ *   sequence; slot_mapping: int64 [num_seqs], its slot. The step's contract:
+ *   row b is sequence b's token at position seq_lens[b] - 1 (slot_mapping[b]
+ *   is that position's slot, or < 0 to write nothing). Everything else is as
+ *   reshape_and_cache followed by paged_attn_decode on `stream`, with the same
+ *   results. Because the library itself writes the cache just ahead of the
+ *   attention kernel, and only those rows, the attention kernel reads its
+ *   inputs and loads every page but the newest token's before the cache write
+ *   has finished (the separate calls must wait for it first).
+ *   All arguments are checked before anything is enqueued.
+ */
+pkv_status paged_attn_decode_step(const void* key, const void* value,
+                                  const int64_t* slot_mapping, void* out, const void* q,
+                                  pkv_dtype q_dtype, void* k_cache, void* v_cache,
+                                  pkv_dtype kv_dtype, const int32_t* block_tables,
+                                  const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int head_dim, int block_size,
+                                  int max_blocks_per_seq, int num_blocks, int max_seq_len,
+                                  float scale, const float* k_scales, const float* v_scales,
+                                  int partition_tokens, float* out_lse, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
 /* Size of the scratch array paged_attn_decode_noalloc uses (32 MiB). */
 #define PKV_NOALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -23,8 +23,9 @@ DEVERR_BITS = {0x1: "block id", 0x2: "slot", 0x4: "seq_len", 0x8: "timeout", 0x1
                0x20: "rotary position", 0x40: "workspace counters not zero"}
 
 # Every symbol include/pkv.h declares.
-EXPORTS = ("paged_attn_decode_workspace_size", "paged_attn_decode", "paged_attn_decode_noalloc",
-           "paged_attn_decode_noalloc_reset", "paged_attn_prefill_chunk", "paged_attn_varlen", "reshape_and_cache",
+EXPORTS = ("paged_attn_decode_workspace_size", "paged_attn_decode", "paged_attn_decode_step",
+           "paged_attn_decode_noalloc", "paged_attn_decode_noalloc_reset",
+           "paged_attn_prefill_chunk", "paged_attn_varlen", "reshape_and_cache",
            "rope_reshape_and_cache", "pkv_get_device_error", "pkv_status_string",
            "pkv_selftest_bounded_wait")
 
@@ -55,6 +56,9 @@ def load(path: str = LIB_PATH):
     L.paged_attn_decode.restype = I
     L.paged_attn_decode.argtypes = [P, P, I, P, P, I, P, P, I, I, I, I, I, I, I, I, F, P, P, I, P,
                                     P, S, P]
+    L.paged_attn_decode_step.restype = I
+    L.paged_attn_decode_step.argtypes = [P, P, P, P, P, I, P, P, I, P, P, I, I, I, I, I, I, I, I,
+                                         F, P, P, I, P, P, S, P]
     L.paged_attn_decode_noalloc.restype = I
     L.paged_attn_decode_noalloc.argtypes = [P, P, I, P, P, I, P, P, I, I, I, I, I, I, I, I, F, P,
                                             P, I, P, P]
@@ -147,6 +151,39 @@ def paged_attn_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
         _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream))
     _check("paged_attn_decode", st)
+
+
+def paged_attn_decode_step(key: torch.Tensor, value: torch.Tensor, slot_mapping: torch.Tensor,
+                           out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                           v_cache: torch.Tensor, block_tables: torch.Tensor,
+                           seq_lens: torch.Tensor, scale: float, max_seq_len: int,
+                           k_scales: Optional[torch.Tensor] = None,
+                           v_scales: Optional[torch.Tensor] = None, partition_tokens: int = 0,
+                           out_lse: Optional[torch.Tensor] = None,
+                           workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """One decode step: key/value[B, Hkv, D] (each sequence's new token, at
+    position seq_lens[b] - 1) written to their slots, then decode attention of
+    q[B, Hq, D] into out, in one call (the attention kernel starts before the
+    cache write has finished). Same workspace rule as paged_attn_decode."""
+    B, Hq, D = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    assert d2 == D and out.shape == q.shape and out.dtype == q.dtype
+    assert key.shape == (B, hkv, D) and value.shape == key.shape and key.dtype == q.dtype
+    assert slot_mapping.dtype == torch.int64 and slot_mapping.shape[0] == B
+    assert block_tables.dtype == torch.int32 and seq_lens.dtype == torch.int32
+    if workspace is None:
+        ws = paged_attn_decode_workspace_size(B, Hq, hkv, D, max_seq_len, partition_tokens)
+        workspace = torch.zeros(max(ws, 256), dtype=torch.uint8, device=q.device)
+    st = load().paged_attn_decode_step(
+        _dev_ptr(key, "key"), _dev_ptr(value, "value"), _dev_ptr(slot_mapping, "slot_mapping"),
+        _dev_ptr(out, "out"), _dev_ptr(q, "q"), dtype_code(q), _dev_ptr(k_cache, "k_cache"),
+        _dev_ptr(v_cache, "v_cache"), dtype_code(k_cache), _dev_ptr(block_tables, "block_tables"),
+        _dev_ptr(seq_lens, "seq_lens"), B, Hq, hkv, D, bs, block_tables.shape[1], nb,
+        int(max_seq_len), float(scale), _dev_ptr(k_scales, "k_scales"),
+        _dev_ptr(v_scales, "v_scales"), int(partition_tokens), _dev_ptr(out_lse, "out_lse"),
+        _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    _check("paged_attn_decode_step", st)
 
 
 def paged_attn_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,

@@ -14,6 +14,7 @@
 #include "../../include/pkv.h"
 #pragma GCC visibility pop
 #include "launch.h"
+#include "plan.h"
 #include "ptx.cuh"
 
 namespace pkv {
@@ -121,53 +122,6 @@ bool make_kv_tmap(CUtensorMap* m, const void* base, pkv_dtype dt, int D, int Hkv
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
-// Split-KV plan of a decode call. With blocks of 16 tokens or more the flat
-// warp schedule runs (decode_flat.cuh): an explicit partition size makes
-// partitions of that many tokens the units of work, each written to its own
-// slot; the automatic split cuts the batch's pages into equal runs, one per
-// warp, so a unit's slots are at most one per warp. Blocks of fewer than 16
-// tokens take the per-partition kernel, whose automatic partition is the
-// smallest power of two from 512 to 2048 tokens that keeps the launch at
-// about 3 waves of resident CTAs when contexts average half the maximum
-// (below 512 tokens its per-CTA start and merge cost more than the extra
-// parallelism gives back).
-// Workspace: [range claims 2 u64 | done counters B*Hkv u64 | merge-group
-// counters, one u64 per slot | slot outputs rows*D fp32 | slot log2-sum-exps
-// rows fp32], each region 256-byte aligned, with slots = max(B*Hkv*max_parts,
-// B*Hkv + ranges of a full grid) and rows = G * slots.
-struct DecodePlan {
-  int part, max_parts;
-  size_t off_done, off_done1, off_o, off_lse, bytes;
-};
-
-DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                       int max_seq_len, int partition_tokens, int sms) {
-  DecodePlan pl{};
-  if (sms <= 0) sms = 148;
-  if (partition_tokens > 0) {
-    pl.part = partition_tokens;
-  } else {
-    const int64_t est = (int64_t)num_seqs * num_kv_heads * std::max(1, max_seq_len / 2);
-    const int64_t target = (int64_t)sms * kDecodeWorkers * 3;
-    pl.part = 512;
-    while (pl.part < 2048 && est / pl.part > target) pl.part *= 2;
-  }
-  pl.max_parts = std::max(1, (max_seq_len + pl.part - 1) / pl.part);
-  const size_t units = (size_t)num_seqs * num_kv_heads;
-  const size_t flat_slots =
-      units + (size_t)sms * kDecodeWorkers * kDecodeWarps * kFlatRangesPerWarp;
-  const size_t slots = std::max(units * (size_t)pl.max_parts, flat_slots);
-  const size_t rows = slots * (size_t)(num_q_heads / num_kv_heads);
-  pl.off_done = 256;
-  pl.off_done1 = pl.off_done + align256(units * 8);
-  pl.off_o = pl.off_done1 + align256(slots * 8);
-  pl.off_lse = pl.off_o + align256(rows * head_dim * sizeof(float));
-  pl.bytes = pl.off_lse + align256(rows * sizeof(float));
-  return pl;
-}
 
 bool valid_dtypes(pkv_dtype q, pkv_dtype kv) {
   if (q != PKV_F16 && q != PKV_BF16) return false;
@@ -317,10 +271,15 @@ pkv_status decode_setup(void* out, const void* q, pkv_dtype q_dtype, const void*
 // reading anything (behind a cache write: its launch overlaps the write);
 // without, it runs beside it (behind the prefill of the same step, whose
 // inputs it does not touch).
-pkv_status decode_launch(const DecodeCall& c, cudaStream_t stream, bool beside_prior) {
+// early: the kernel just ahead on the stream is this library's cache write of
+// each sequence's newest token (paged_attn_decode_step), so the decode reads
+// its inputs and loads every other page before waiting for it.
+pkv_status decode_launch(const DecodeCall& c, cudaStream_t stream, bool beside_prior,
+                         bool early = false) {
   if (c.empty) return PKV_OK;
   DecodeParams p = c.p;
   p.wait_prior = beside_prior ? 0 : 1;
+  p.early = early ? 1 : 0;
   return launch_decode(p, c.head_dim, c.q_dtype, c.kv_dtype, c.tmK, c.tmV, stream, true);
 }
 
@@ -425,6 +384,33 @@ pkv_status paged_attn_decode(void* out, const void* q, pkv_dtype q_dtype, const 
   if (st != PKV_OK || c.empty) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   return decode_launch(c, s, false);
+}
+
+pkv_status paged_attn_decode_step(const void* key, const void* value,
+                                  const int64_t* slot_mapping, void* out, const void* q,
+                                  pkv_dtype q_dtype, void* k_cache, void* v_cache,
+                                  pkv_dtype kv_dtype, const int32_t* block_tables,
+                                  const int32_t* seq_lens, int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int head_dim, int block_size,
+                                  int max_blocks_per_seq, int num_blocks, int max_seq_len,
+                                  float scale, const float* k_scales, const float* v_scales,
+                                  int partition_tokens, float* out_lse, void* workspace,
+                                  size_t workspace_bytes, void* stream) {
+  DecodeCall c;
+  pkv_status st = decode_setup(out, q, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
+                               seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                               block_size, max_blocks_per_seq, num_blocks, max_seq_len, scale,
+                               k_scales, v_scales, partition_tokens, out_lse, workspace,
+                               workspace_bytes, &c);
+  if (st != PKV_OK) return st;
+  // checked in full before anything is enqueued
+  if (num_seqs > 0 && (!key || !value || !slot_mapping || !aligned16(key) || !aligned16(value)))
+    return PKV_ERR_INVALID_ARG;
+  st = reshape_and_cache(key, value, q_dtype, k_cache, v_cache, kv_dtype, slot_mapping, num_seqs,
+                         num_kv_heads, head_dim, block_size, num_blocks, k_scales, v_scales,
+                         stream);
+  if (st != PKV_OK || c.empty) return st;
+  return decode_launch(c, reinterpret_cast<cudaStream_t>(stream), false, true);
 }
 
 pkv_status paged_attn_prefill_chunk(void* out, const void* q, pkv_dtype q_dtype,

@@ -64,8 +64,10 @@ __global__ void __launch_bounds__(NW * 32)
   const int part_idx = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int G = p.G;
   // launched as a programmatic dependent: the CTA is resident early, and
-  // reads nothing before the kernel ahead of it (the cache write) is done
-  if (p.wait_prior) griddep_wait();
+  // reads nothing before the kernel ahead of it (the cache write) is done;
+  // in the early-start mode it reads what that kernel does not write first
+  const bool early = !GATHER && p.early != 0;
+  if (p.wait_prior && !early) griddep_wait();
 
   int ctx = p.seq_lens[b];
   const int cap = min(p.max_seq_len, p.max_blocks << p.bs_log2);
@@ -169,9 +171,19 @@ __global__ void __launch_bounds__(NW * 32)
       }
     }
   };
+  // the page holding the newest token (position ctx - 1) is written by the
+  // kernel ahead: in the early-start mode its load waits for that kernel
+  const int new_pg = ctx > 0 ? (ctx - 1) / kBS - page0 : -1;
+  const int held = (early && new_pg >= 0 && new_pg < npages && new_pg % NW == warp &&
+                    new_pg / NW < NST) ? new_pg / NW : -1;
   if (GATHER || lane == 0)
-    for (int k = 0; k < NST && k < nmine; ++k) issue(k);
+    for (int k = 0; k < NST && k < nmine; ++k)
+      if (k != held) issue(k);
   int issued = min(NST, nmine);
+  if (early && p.wait_prior) {
+    griddep_wait();
+    if (held >= 0 && lane == 0) issue(held);
+  }
 
   // ---- query fragments (heads in N), straight from global memory --------------------
   const uint16_t* qb = static_cast<const uint16_t*>(p.q) + ((int64_t)b * p.Hq + h * G) * D;

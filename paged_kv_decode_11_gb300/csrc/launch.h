@@ -51,6 +51,11 @@ struct DecodeParams {
   int part, max_parts;        // partition size (tokens) and partitions per sequence
   float qk_scale_log2;        // scale * log2(e)
   int wait_prior;             // wait for the grids ahead of it on the stream before reading
+  // early start (per-partition kernel, TMA pages): the kernel ahead of it is
+  // known to write nothing but the cache rows of each sequence's newest token
+  // (the library's own cache write), so everything else is read, and every
+  // other page is loaded, before the wait
+  int early;
   // flat schedule (decode_flat.cuh, blocks of >= 16 tokens): the batch's
   // (sequence, KV head, page) space is cut into equal runs, one per warp
   int explicit_parts;         // 1: partitions of `part` tokens are the units of work

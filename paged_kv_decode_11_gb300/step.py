@@ -87,8 +87,13 @@ class DecodeStep:
                             out_lse=self.lse, workspace=self.workspace, stream=stream)
 
     def run(self, stream=None):
-        self.write_cache(stream)
-        self.attend(stream)
+        """The whole step in one call (paged_attn_decode_step): the cache write
+        of the new tokens, then attention, which starts before the write ends."""
+        B.paged_attn_decode_step(self.new_k, self.new_v, self.new_slots, self.out, self.q,
+                                 self.k_cache, self.v_cache, self.block_tables, self.seq_lens,
+                                 self.scale, self.max_seq_len, self.k_scales, self.v_scales,
+                                 partition_tokens=self.partition_tokens, out_lse=self.lse,
+                                 workspace=self.workspace, stream=stream)
 
     # host <-> device traffic of one step, for end-to-end timing: the inputs
     # live in one buffer, so one copy brings them all

@@ -35,6 +35,24 @@ def test_header_declares_the_abi():
     assert header_functions() == sorted(_binding.EXPORTS)
 
 
+def header_param_counts():
+    """Number of parameters of every function the header declares."""
+    txt = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    counts = {}
+    for m in re.finditer(r"\b([a-z_][a-z0-9_]*)\s*\(([^;{]*?)\)\s*;", txt):
+        params = m.group(2).strip()
+        counts[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return counts
+
+
+def test_binding_signatures_match_the_header(lib):
+    counts = header_param_counts()
+    for name in _binding.EXPORTS:
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None, name
+        assert len(fn.argtypes) == counts[name], (name, len(fn.argtypes), counts[name])
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in header_functions():
         assert hasattr(lib, name), name
