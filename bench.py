@@ -195,7 +195,7 @@ def source_hash() -> str:
 
 def profile_traffic(config: str):
     """DRAM bytes per decode call of this workload, as ncu measured them
-    (profiles/decode_traffic.json, written by profiles/decode_traffic.py),
+    (profiles/decode_traffic.json, written by `bench.py --record-traffic`),
     if they were taken on the current decode sources; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
@@ -252,6 +252,36 @@ def record_traffic(args):
         json.dump(data, f, indent=1, sort_keys=True)
         f.write("\n")
     print(json.dumps({args.config: data[args.config]}))
+
+
+class L2Flush:
+    """Evicts everything from L2 between timed iterations (untimed): a write
+    of a buffer twice the L2's size, then a read of a second one, so the
+    write's dirty lines go back to HBM here and the L2 is left holding clean
+    lines that the next iteration can drop for free."""
+
+    def __init__(self):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        self.acc = torch.zeros((), dtype=torch.float32, device="cuda")
+
+    def __call__(self, i: int):
+        self.w.fill_(i & 0xFF)
+        self.acc.copy_(self.r.sum())
+
+    @staticmethod
+    def describe(what: str) -> str:
+        return (f"flushed between timed {what}: a {L2_FLUSH_BYTES >> 20} MiB write, then a "
+                f"{L2_FLUSH_BYTES >> 20} MiB read, so no dirty lines remain (untimed)")
+
+
+def decode_kernel_name(case) -> str:
+    """The kernel a decode call of this workload launches (decode.cu's routing)."""
+    if case.BS < 16:
+        return "decode_kernel, cp.async gather instantiation (one launch per decode call)"
+    if case.partition_tokens:
+        return "decode_flat_kernel (one launch per decode call)"
+    return "decode_kernel (one launch per decode call)"
 
 
 def measured_hbm_peak():
@@ -398,7 +428,7 @@ def run_ours(args):
     # reshape_and_cache + one decode launch (+ one prefill launch)
     launches_per_step = 2 + (1 if case.prefill is not None else 0)
     kv_bytes, kv_logical = step_kv_bytes(case)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     stream = torch.cuda.current_stream()
 
     def one_step():
@@ -419,7 +449,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     t0 = time.time()
     for i in range(K):
-        flush.fill_(i & 0xFF)                       # evict the previous step from L2
+        flush(i)                                    # evict the previous step from L2
         ev[i][0].record(stream)
         one_step()                                  # the step's own call(s)
         ev[i][1].record(stream)
@@ -433,7 +463,7 @@ def run_ours(args):
         ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(K)]
         for i in range(K):
-            flush.fill_(i & 0xFF)
+            flush(i)
             step.write_cache(stream)
             ev2[i][0].record(stream)
             step.attend(stream)
@@ -492,14 +522,14 @@ def run_ours(args):
                 "global_batch": int(total_seqs),
                 "kv_bytes_per_step": int(kv_bytes),
                 "kv_bytes_logical_per_step": int(kv_logical),
-                "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed); "
-                      f"the step reads {kv_bytes / 1e6:.0f} MB of KV",
+                "l2": L2Flush.describe("steps") +
+                      f"; the step reads {kv_bytes / 1e6:.0f} MB of KV",
                 "parallelism": f"replicas x{world} (independent batch per GPU)",
             },
             "seqs_per_s_per_layer": round(total_seqs / (ms / 1e3), 1),
             "pct_of_nominal_hbm": round(100 * value / world / NOMINAL_HBM_GBS, 2),
             "roofline": {
-                "kernel": "decode_kernel (one launch per decode call)",
+                "kernel": decode_kernel_name(case),
                 "bound": "hbm",
                 "achieved": round(achieved, 2) if achieved else None,
                 "peak": peak,
@@ -546,7 +576,7 @@ def measure_graph(step, stream, args, world, kv_bytes, flush, launches):
     torch.cuda.synchronize()
     cur = torch.cuda.current_stream()
     for i in range(K):
-        flush.fill_(i & 0xFF)
+        flush(i)
         ev[i][0].record(cur)
         g.replay()
         ev[i][1].record(cur)
@@ -584,7 +614,7 @@ def measure_e2e(step, stream, args, world, kv_bytes, flush):
     barrier(world)
     torch.cuda.synchronize()
     for i in range(K):
-        flush.fill_(i & 0xFF)
+        flush(i)
         ev[i][0].record(stream)
         e2e_step()
         ev[i][1].record(stream)
@@ -706,7 +736,7 @@ def run_prefill_only(args):
                         torch.from_numpy(case.new_slots).cuda(), ks, vs)
     step = MixedStep.from_case(case, kc, vc, mode="streams")
     stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     for _ in range(args.warmup):
         step.prefill(stream)
     torch.cuda.synchronize()
@@ -721,7 +751,7 @@ def run_prefill_only(args):
     torch.cuda.synchronize()
     t0 = time.time()
     for i in range(K):
-        flush.fill_(i & 0xFF)
+        flush(i)
         ev[i][0].record(stream)
         step.prefill(stream)
         ev[i][1].record(stream)
@@ -750,8 +780,7 @@ def run_prefill_only(args):
                                    f"{'E4M3' if case.kv_fp8 else case.dtype} KV, "
                                    f"{case.dtype} q, block 16",
                        "flops_per_call": flops,
-                       "l2": f"flushed between timed calls ({L2_FLUSH_BYTES >> 20} MiB write, "
-                             f"untimed)"},
+                       "l2": L2Flush.describe("calls")},
             "roofline": {"kernel": "prefill_tc_kernel (one launch per call)", "bound": "tensor",
                          "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                          "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None},

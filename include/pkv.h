@@ -58,6 +58,14 @@
  *  - Cache slots past a sequence's context (the rest of its last block) may
  *    hold anything, NaN included: they are read with weight 0 and their
  *    values are zeroed before they meet that weight.
+ *  - E4M3 caches run f16 tensor-core MMAs on the codes widened to f16
+ *    (exact). A bf16 q is scaled by a power of two 2^-e, rounded to f16, and
+ *    the scores are multiplied back by 2^e: e is chosen per sequence and KV
+ *    head in decode (per query row in prefill) so that the largest |q|
+ *    element lands in [2^14, 2^15). Any finite bf16 q works (no overflow to
+ *    inf). Elements within 2^-28 of the largest of their group convert
+ *    exactly; smaller ones fall into f16's subnormal range and move by at
+ *    most 2^-39 of the largest.
  *  - Supported: D in {64, 128, 256}; BS a power of two from 1 to 64 (decode
  *    and the cache writes; prefill, and decode at D = 256, need BS >= 16);
  *    G <= 16 (G <= 8 at D = 256); q dtype F16 or BF16; KV
@@ -249,7 +257,7 @@ pkv_status paged_attn_decode_noalloc_reset(void* stream);
  *   half of the SMs, a cluster of two CTAs per tile, each over half of the
  *   tile's keys, merged by log-sum-exp on chip (tensor-core kernel: 16-bit
  *   caches at D 64/128/256, E4M3 caches at D 64/128). With an E4M3 cache a
- *   bf16 q is rounded to f16 for the MMAs (exact for |q| in [2^-14, 65504]).
+ *   bf16 q goes to f16 MMAs as described at the top of this file.
  */
 pkv_status paged_attn_prefill_chunk(void* out, const void* q,
                                     pkv_dtype q_dtype, const void* k_cache,
