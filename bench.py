@@ -178,7 +178,7 @@ class ClockSampler:
 
 # The device code the decode kernels are built from and their partition
 # planner: a traffic figure ncu took stays valid while none of these changes.
-DECODE_SOURCES = ("common.cuh", "decode.cu", "decode_flat.cuh", "decode_frags.cuh",
+DECODE_SOURCES = ("common.cuh", "decode.cu", "decode_frags.cuh",
                   "decode_kernel.cuh", "launch.h", "plan.h", "ptx.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
 
@@ -225,7 +225,7 @@ def record_traffic(args):
         if len(r) < len(hdr):
             continue
         name = r[col["Kernel Name"]]
-        if "decode_kernel" not in name and "decode_flat_kernel" not in name:
+        if "decode_kernel" not in name:
             continue
         metric = r[col["Metric Name"]]
         if metric not in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
@@ -279,8 +279,6 @@ def decode_kernel_name(case) -> str:
     """The kernel a decode call of this workload launches (decode.cu's routing)."""
     if case.BS < 16:
         return "decode_kernel, cp.async gather instantiation (one launch per decode call)"
-    if case.partition_tokens:
-        return "decode_flat_kernel (one launch per decode call)"
     return "decode_kernel (one launch per decode call)"
 
 

@@ -240,9 +240,7 @@ pkv_status decode_setup(void* out, const void* q, pkv_dtype q_dtype, const void*
   p.k_scales = k_scales;
   p.v_scales = v_scales;
   p.out_lse = out_lse;
-  p.claims = reinterpret_cast<unsigned long long*>(ws);
   p.done = reinterpret_cast<unsigned long long*>(ws + pl.off_done);
-  p.done1 = reinterpret_cast<unsigned long long*>(ws + pl.off_done1);
   p.ws_o = reinterpret_cast<float*>(ws + pl.off_o);
   p.ws_lse = reinterpret_cast<float*>(ws + pl.off_lse);
   p.err = err;
@@ -257,12 +255,11 @@ pkv_status decode_setup(void* out, const void* q, pkv_dtype q_dtype, const void*
   p.bs_log2 = bs_log2;
   p.part = pl.part;
   p.max_parts = pl.max_parts;
+  p.wpart = warp_partition_tokens(partition_tokens, bs_log2);
+  if (p.wpart > 0) p.part = p.wpart * kDecodeWarps;
+  p.grid_parts = std::max(1, (max_seq_len + p.part - 1) / p.part);
   p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   p.wait_prior = 1;
-  p.explicit_parts = partition_tokens > 0 ? 1 : 0;
-  p.min_atoms = kFlatMinPages;
-  p.cap = (int)std::min<int64_t>(max_seq_len, (int64_t)max_blocks_per_seq << bs_log2);
-  p.ppp = partition_tokens > 0 ? partition_tokens / 16 : 0;     // 16-token pages
   return PKV_OK;
 }
 

@@ -1,11 +1,8 @@
 // decode.cu — paged-KV decode attention: split-KV partitions and their
-// log-sum-exp merge in one kernel launch. With an automatic split, one CTA
-// per (partition, KV head, sequence) (decode_kernel.cuh; the hardware hands
-// CTAs to SMs as they free up, which balances uneven SMs for free); with an
-// explicit partition size, the flat warp schedule (decode_flat.cuh), which
-// runs many short partitions per warp without a CTA start-up each. Blocks of
-// fewer than 16 tokens go to the gather instantiation in decode_gather.cu.
-#include "decode_flat.cuh"
+// log-sum-exp merge in one kernel launch, one CTA per (CTA partition, KV
+// head, sequence) (decode_kernel.cuh; the hardware hands CTAs to SMs as they
+// free up, which balances uneven SMs for free). Blocks of fewer than 16
+// tokens go to the gather instantiation in decode_gather.cu.
 #include "decode_kernel.cuh"
 
 namespace pkv {
@@ -15,14 +12,8 @@ pkv_status launch_decode(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                          cudaStream_t stream, bool programmatic) {
   if (p.bs_log2 < 4)
     return launch_decode_gather(p, head_dim, q_dtype, kv_dtype, stream, programmatic);
-  if (!p.explicit_parts)
-    return launch_decode_mode<false>(p, head_dim, q_dtype, kv_dtype, tmK, tmV, stream,
-                                     programmatic);
-  if (head_dim == 256)
-    return launch_flat_d<256>(p, q_dtype, kv_dtype, tmK, tmV, stream, programmatic);
-  if (head_dim == 128)
-    return launch_flat_d<128>(p, q_dtype, kv_dtype, tmK, tmV, stream, programmatic);
-  return launch_flat_d<64>(p, q_dtype, kv_dtype, tmK, tmV, stream, programmatic);
+  return launch_decode_mode<false>(p, head_dim, q_dtype, kv_dtype, tmK, tmV, stream,
+                                   programmatic);
 }
 
 }  // namespace pkv

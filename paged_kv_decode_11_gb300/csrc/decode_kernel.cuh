@@ -9,20 +9,26 @@
 // thread blocks") and the log-sum-exp merge of partial attention (rapid_llm
 // README, feature table, "Decode context parallelism").
 //
-// Work decomposition: one CTA per (partition, KV head, sequence); a
-// partition is `part` consecutive tokens of one context. The CTA's NW warps
-// take the partition's pages round-robin, and each warp runs its own NST-deep
+// Work decomposition: one CTA per (CTA partition, KV head, sequence); a CTA
+// partition is `part` consecutive tokens of one context. With warp
+// partitions (an explicit partition size, pages loaded by TMA) warp w takes
+// the w-th run of `wpart` tokens of it, one split-KV partition with its own
+// online softmax; otherwise the CTA's NW warps take the CTA partition's
+// pages round-robin. Each warp runs its own NST-deep
 // ring of TMA loads (one K page + one V page per stage, completion on an
 // mbarrier), issued by the warp itself as soon as it has read a stage, so
 // every warp keeps its own stream of requests in flight. The GQA group's
 // query heads sit in the MMA N dimension (decode_frags.cuh), so each K/V byte
 // is read from HBM once per call. Each warp runs an online softmax in the
 // log2 domain; at the end the warps are merged through shared memory (the
-// ring's space, then free). A sequence with one partition is written out
-// directly. Otherwise the partition's normalised output and its log2-sum-exp
-// go to the workspace and a per-(sequence, KV head) counter is bumped; the
-// CTA whose bump completes the count merges the partitions:
+// ring's space, then free) by log-sum-exp. A sequence with one CTA partition
+// is written out directly. Otherwise the CTA partition's normalised output
+// and its log2-sum-exp go to the workspace and a per-(sequence, KV head)
+// counter is bumped; the CTA whose bump completes the count merges the CTA
+// partitions:
 //   LSE = log2 sum_p 2^{lse_p},  out = v_scale * sum_p 2^{lse_p - LSE} o_p.
+// (With warp partitions the split-KV partitions are thus merged in two
+// levels, the LSE merge being associative.)
 #pragma once
 #include <cuda.h>
 #include "decode_frags.cuh"
@@ -81,6 +87,9 @@ __global__ void __launch_bounds__(NW * 32)
   const int tok1 = min(ctx, tok0 + p.part);
   const int npages = (tok1 - tok0 + kBS - 1) / kBS;
   const int page0 = tok0 / kBS;
+  // warp partitions: warp w takes the CTA's pages [w * ppw, (w + 1) * ppw);
+  // otherwise (ppw = 0) pages w, w + NW, w + 2 NW, ...
+  const int ppw = GATHER ? 0 : p.wpart / kBS;
 
   const uint32_t raw_base = smem_u32(smem_raw);
   const uint32_t base = (raw_base + 1023u) & ~1023u;
@@ -132,7 +141,10 @@ __global__ void __launch_bounds__(NW * 32)
   // swizzled layout, each lane's copies completing on the stage's mbarrier ----
   const uint32_t wbase = base + warp * NST * STAGE;
   uint8_t* wbasep = basep + warp * NST * STAGE;
-  const int nmine = warp < npages ? (npages - warp + NW - 1) / NW : 0;
+  const int nmine = ppw ? max(0, min(ppw, npages - warp * ppw))
+                       : (warp < npages ? (npages - warp + NW - 1) / NW : 0);
+  // the CTA's page index of this warp's k-th page
+  auto page_of = [&](int k) { return ppw ? warp * ppw + k : warp + NW * k; };
   const uint8_t* kcache = static_cast<const uint8_t*>(p.k_cache);
   const uint8_t* vcache = static_cast<const uint8_t*>(p.v_cache);
   // KV pages are read once per call: mark them first to go from L2, so they
@@ -143,7 +155,7 @@ __global__ void __launch_bounds__(NW * 32)
     uint64_t* bar = &bars[warp][st];
     uint8_t* dst = wbasep + st * STAGE;
     if constexpr (GATHER) {
-      const int* rows = s_ids + (warp + NW * k) * kBS;
+      const int* rows = s_ids + page_of(k) * kBS;
       constexpr int CPR = Geo::ROW_BYTES / 16;             // 16-byte chunks per row
       // Copies a lane keeps in flight: NST stages of K and V. Configurations
       // up to 32 ran on GB300; one with 64 (bf16, D = 256, two stages) raised
@@ -160,7 +172,7 @@ __global__ void __launch_bounds__(NW * 32)
       }
       cp_async_mbar_arrive_noinc(bar);
     } else {
-      const int z = s_ids[warp + NW * k];
+      const int z = s_ids[page_of(k)];
       mbar_arrive_expect_tx(bar, STAGE);
 #pragma unroll
       for (int bx = 0; bx < Geo::NBOX; ++bx) {
@@ -174,8 +186,10 @@ __global__ void __launch_bounds__(NW * 32)
   // the page holding the newest token (position ctx - 1) is written by the
   // kernel ahead: in the early-start mode its load waits for that kernel
   const int new_pg = ctx > 0 ? (ctx - 1) / kBS - page0 : -1;
-  const int held = (early && new_pg >= 0 && new_pg < npages && new_pg % NW == warp &&
-                    new_pg / NW < NST) ? new_pg / NW : -1;
+  const int new_k = ppw ? (new_pg / ppw == warp ? new_pg % ppw : -1)
+                        : (new_pg % NW == warp ? new_pg / NW : -1);
+  const int held = (early && new_pg >= 0 && new_pg < npages && new_k >= 0 && new_k < NST)
+                       ? new_k : -1;
   if (GATHER || lane == 0)
     for (int k = 0; k < NST && k < nmine; ++k)
       if (k != held) issue(k);
@@ -224,7 +238,7 @@ __global__ void __launch_bounds__(NW * 32)
     }
     const uint32_t kpage = wbase + st * STAGE;
     const uint32_t vpage = kpage + Geo::PAGE_BYTES;
-    const int tbase = tok0 + (warp + NW * k) * kBS;
+    const int tbase = tok0 + page_of(k) * kBS;
     if (tok1 - tbase < kBS) {
       // the last page of the context: its rows past the end get weight 0, and
       // whatever they hold must not turn that into NaN, so zero them in V
@@ -492,6 +506,7 @@ static pkv_status launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK,
                                   bool programmatic) {
   constexpr int NW = PKV_DECODE_NW;
   constexpr int NST = (KV == KV_E4M3) ? PKV_DECODE_NST_E4M3 : PKV_DECODE_NST_16;
+  static_assert(NW == kDecodeWarps, "warp partitions are planned for kDecodeWarps warps");
   using Cfg = DecodeCfg<D, KV, NT, NW, NST>;
   auto kern = decode_kernel<D, KV, QBF16, NT, NW, NST, GATHER>;
   int dev = 0;
@@ -503,7 +518,7 @@ static pkv_status launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK,
       return PKV_ERR_CUDA;
     attr_set[dev] = true;
   }
-  dim3 grid(p.max_parts, p.Hkv, p.B);
+  dim3 grid(p.grid_parts, p.Hkv, p.B);
   if (programmatic) {
     // may start while the previous kernel on the stream still runs (it
     // reads nothing that kernel writes)

@@ -15,19 +15,6 @@ constexpr int kMaxPartitionTokens = 8192;
 constexpr int kGatherMaxPartitionTokens = 2048;   // split-KV partition cap (block ids staged in smem)
 constexpr int kDecodeWorkers = 4;           // resident decode CTAs per SM assumed by the planner
 constexpr int kDecodeWarps = 4;             // warps per decode CTA
-// Fewest pages a warp of the flat decode takes when the split is automatic:
-// below this the per-warp start (query load, page lookups, first page) and
-// the partial it writes cost more than the extra parallelism gives back.
-constexpr int kFlatMinPages = 8;
-// Flat decode ranges: each warp's first range holds kFlatStaticPct percent of
-// its even share of the batch; the rest is cut into about kFlatTailChunks
-// chunks per warp that warps claim as they finish, so the warps that run
-// faster take more of the tail. At most 1 + kFlatTailChunks ranges per warp.
-constexpr int kFlatStaticPct = 85;
-constexpr int kFlatTailChunks = 2;
-constexpr int kFlatRangesPerWarp = 1 + kFlatTailChunks;
-// Slots merged in one step: units with more merge in two levels.
-constexpr int kMergeGroup = 16;
 
 struct DecodeParams {
   void* out;
@@ -40,15 +27,17 @@ struct DecodeParams {
   const float* v_scales;
   float* out_lse;
   unsigned long long* done;   // [B * Hkv] finished-partition counters (zero between calls)
-  unsigned long long* done1;  // flat schedule: first-level merge-group counters, one per slot
-  unsigned long long* claims; // flat schedule: [range claims, warps done claiming]
   float* ws_o;                // [B * Hq, max_parts, D] fp32 partition outputs (normalised)
   float* ws_lse;              // [B * Hq, max_parts]    fp32 partition log2-sum-exp
   unsigned int* err;          // device error word
   int B, Hq, Hkv, G, max_blocks, num_blocks, max_seq_len;
   int ppb_shift;              // log2(block_size / 16): 16-token pages per block (TMA mode)
   int bs_log2;                // log2(block_size)
-  int part, max_parts;        // partition size (tokens) and partitions per sequence
+  int part, max_parts;        // CTA partition size (tokens) and workspace slots per sequence
+  int wpart;                  // > 0: each warp of a CTA reduces its own partition of
+                              // this many tokens (part = warps * wpart); 0: the warps
+                              // take the CTA partition's pages round-robin
+  int grid_parts;             // CTAs per (sequence, KV head) in the grid
   float qk_scale_log2;        // scale * log2(e)
   int wait_prior;             // wait for the grids ahead of it on the stream before reading
   // early start (per-partition kernel, TMA pages): the kernel ahead of it is
@@ -56,12 +45,6 @@ struct DecodeParams {
   // (the library's own cache write), so everything else is read, and every
   // other page is loaded, before the wait
   int early;
-  // flat schedule (decode_flat.cuh, blocks of >= 16 tokens): the batch's
-  // (sequence, KV head, page) space is cut into equal runs, one per warp
-  int explicit_parts;         // 1: partitions of `part` tokens are the units of work
-  int min_atoms;              // automatic split: fewest pages a warp takes
-  int cap;                    // min(max_seq_len, max_blocks * block_size): longest context
-  int ppp;                    // pages per partition (explicit split), 0 = automatic
 };
 
 struct PrefillParams {

@@ -108,21 +108,15 @@ def test_decode_workspace_check(lib):
 
 
 def test_workspace_size_formula(lib):
-    # [range claims: 2 words | done counters: B*Hkv words | merge-group counters:
-    # one word per slot | slot outputs: G*slots rows of D fp32 | slot
-    # log2-sum-exps: G*slots fp32], each region 256-aligned, where slots is the
-    # larger of B*Hkv*parts (parts = ceil(max_seq_len / partition)) and B*Hkv
-    # plus the ranges of a full grid (3 per warp, 4 CTAs of 4 warps per SM;
-    # with no GPU visible the library assumes 148 SMs)
+    # [done counters: B*Hkv words | partition outputs: B*Hq*parts rows of D
+    # fp32 | partition log2-sum-exps: B*Hq*parts fp32], each region
+    # 256-aligned, parts = ceil(max_seq_len / partition)
     def a256(x):
         return (x + 255) // 256 * 256
-    grid_ranges = 148 * 4 * 4 * 3
 
     def want(B, Hq, Hkv, D, parts):
-        units, G = B * Hkv, Hq // Hkv
-        slots = max(units * parts, units + grid_ranges)
-        return 256 + a256(units * 8) + a256(slots * 8) + a256(G * slots * D * 4) + \
-            a256(G * slots * 4)
+        rows = B * Hq * parts
+        return a256(B * Hkv * 8) + a256(rows * D * 4) + a256(rows * 4)
     assert P.paged_attn_decode_workspace_size(128, 32, 8, 128, 8192, 1024) == \
         want(128, 32, 8, 128, 8)
     assert P.paged_attn_decode_workspace_size(4, 8, 2, 64, 100, 256) == want(4, 8, 2, 64, 1)

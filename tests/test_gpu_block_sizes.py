@@ -159,11 +159,12 @@ def test_gather_cache_write_bit_exact(BS, kv):
 
 @pytest.mark.parametrize("kv", ["same", "fp8"])
 def test_decode_bit_identical_within_each_page_path(kv):
-    # blocks below a page are gathered row by row (the per-partition kernel),
-    # blocks of a page or more are read page by page (the flat kernel): each
-    # path walks the same 16-token pages in the same order for every block
-    # size, so within a path the results are bit-identical; both paths agree
-    # with the oracle
+    # blocks below a page are gathered row by row (the warps of a CTA take
+    # its partition's pages in turn), blocks of a page or more are read page
+    # by page by TMA (each warp reduces a partition of its own): each path
+    # walks the same 16-token pages in the same order for every block size,
+    # so within a path the results are bit-identical; both paths agree with
+    # the oracle
     outs = {}
     for BS in (1, 4, 16, 32, 64):
         c = _case(BS, kv)
