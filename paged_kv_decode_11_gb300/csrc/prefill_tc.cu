@@ -44,34 +44,62 @@
 namespace pkv {
 
 constexpr int kTcRows = 128;                  // query rows per CTA (MMA M)
-constexpr int kTcKeys = 64;                   // keys per tile (S MMA N)
-constexpr int kTcPages = kTcKeys / kBS;
 constexpr float kRescaleLog2 = 8.f;           // reference-max slack (log2 units)
 
 // NG softmax groups of four warps (two up to D = 128; one at D = 256, whose O
-// takes 256 TMEM columns), then the K producer, MMA and V producer warps.
-// KV8: an E4M3 cache. Its tiles land by TMA in an NSS-deep staging ring and
-// the producer warps convert them to f16 (exact: E4M3 is a subset of f16)
-// into the rings the MMAs read.
-template <int D, int NST, bool KV8 = false>
+// takes 256 TMEM columns), then PK K producer warps, the MMA warp and PV V
+// producer warps. One warp's TMA loads complete at about 16 GB/s for
+// page-sized (2 KB) boxes on GB300, whatever the ring depth, and the rate
+// grows with the number of issuing warps: with 128-key tiles a 16-bit cache
+// has 4 K and 3 V producers, which take the boxes of a tile in turn, and the
+// producer warpgroups hand registers to the softmax ones (REALLOC). KV8: an
+// E4M3 cache. Its tiles land by TMA in an NSS-deep staging ring and one
+// producer warp per operand converts them to f16 (exact: E4M3 is a subset
+// of f16) into the rings the MMAs read.
+// ALONE: nothing else runs on the GPU beside this grid (a chunk call of its
+// own, not the prefill half of a varlen step).
+template <int D, int NST, bool KV8 = false, bool ALONE = true>
 struct PrefillTcCfg {
   static constexpr int NG = D <= 128 ? 2 : 1;
-  static constexpr int THREADS = NG * kTcRows + 3 * 32;
-  static constexpr int W_K = 4 * NG, W_MMA = 4 * NG + 1, W_V = 4 * NG + 2;
+  // keys per tile (the S MMA's N): 128 for 16-bit caches at D <= 128 running
+  // alone, with one S buffer (TMEM) and one P buffer (shared) per group; 64
+  // otherwise, with two. Beside a decode grid the 64-key kernel, whose loads
+  // press less on L2, made the varlen step faster (102.7 against 104.4 us on
+  // the mixed step), while alone the 128-key one is faster at every size.
+  static constexpr bool WIDE = ALONE && !KV8 && D <= 128;
+  static constexpr int KEYS = WIDE ? 128 : 64;
+  static constexpr int PAGES = KEYS / kBS;                   // 16-token pages per tile
+  static constexpr int NSB = WIDE ? 1 : 2;                   // S and P buffers per group
+  static constexpr int PK = WIDE ? 4 : 1;
+  static constexpr int PV = WIDE ? 3 : 1;
+  static constexpr int WARPS = 4 * NG + PK + 1 + PV;
+  static constexpr int THREADS = WARPS * 32;
+  static constexpr int W_K = 4 * NG, W_MMA = 4 * NG + PK, W_V = 4 * NG + PK + 1;
+  // 16 warps (4 per SM sub-partition) launch at 128 registers a thread: the
+  // softmax warpgroups rise to REG_SOFTMAX, the K producers (warpgroup 2) and
+  // the MMA warp with the V producers (warpgroup 3) fall to REG_K / REG_MV
+  static constexpr bool REALLOC = WARPS == 16;
+  static constexpr int REG_SOFTMAX = 184, REG_K = 48, REG_MV = 56;
+  static_assert(!REALLOC || (NG == 2 && W_MMA == 12), "warpgroups: 2 softmax, K, MMA + V");
+  // registers the warpgroups hold after the moves; the launcher checks that
+  // the kernel was built to launch with at least this many (512 threads)
+  static constexpr int REG_TOTAL = 256 * REG_SOFTMAX + 128 * (REG_K + REG_MV);
+  static_assert(!REALLOC || REG_TOTAL <= 512 * 128, "more than 16 warps can hold");
   static constexpr int NBOX = D / 64;                        // 128-byte column blocks per row
   static constexpr int Q_BOX = kTcRows * 128;                // one column block of Q
   static constexpr int Q_BYTES = NBOX * Q_BOX;
-  static constexpr int KV_BOX = kTcPages * kBS * 128;        // one column block of a K/V tile
+  static constexpr int KV_BOX = PAGES * kBS * 128;           // one column block of a K/V tile
   static constexpr int KV_BYTES = NBOX * KV_BOX;            // one K (or V) tile
   static constexpr int RING_BYTES = NST * KV_BYTES;          // one ring (K, then V)
-  static constexpr int P_BYTES = kTcRows * 128;              // one P buffer (2 per group)
+  static constexpr int P_CB = kTcRows * 128;                 // 64 keys of a P buffer
+  static constexpr int P_BYTES = (KEYS / 64) * P_CB;         // one P buffer (NSB per group)
   static constexpr int NSS = KV8 ? 4 : 0;                    // staging stages per operand
   static constexpr int STG_PAGE = kBS * D;                   // one E4M3 page
-  static constexpr int STG_BYTES = kTcPages * STG_PAGE;      // one staged E4M3 tile
+  static constexpr int STG_BYTES = PAGES * STG_PAGE;         // one staged E4M3 tile
   static constexpr int SMEM_BYTES =
-      1024 + Q_BYTES + 2 * RING_BYTES + 2 * NG * P_BYTES + 2 * NSS * STG_BYTES;
+      1024 + Q_BYTES + 2 * RING_BYTES + NSB * NG * P_BYTES + 2 * NSS * STG_BYTES;
   static constexpr uint32_t TMEM_COLS = 512;                  // 2 S buffers and O per group
-  static_assert(NG * (2 * kTcKeys + D) <= (int)TMEM_COLS, "tensor memory");
+  static_assert(NG * (NSB * KEYS + D) <= (int)TMEM_COLS, "tensor memory");
 };
 
 __device__ __forceinline__ uint32_t swz128(uint32_t r, uint32_t chunk) {
@@ -153,15 +181,16 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[N]) {
 // KV: the cache type; the MMAs take bf16 operands for a bf16 cache and f16
 // ones otherwise (an E4M3 cache is converted to f16, and bf16 queries with
 // it). QBF16: the query and output type.
-template <int D, int KV, bool QBF16, int NST, int SPLIT>
-__global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 1)
+template <int D, int KV, bool QBF16, int NST, int SPLIT, bool ALONE>
+__global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::THREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
   constexpr bool KV8 = KV == KV_E4M3;
   constexpr bool BF16 = KV == KV_BF16;                  // MMA operand type
-  using Cfg = PrefillTcCfg<D, NST, KV8>;
+  using Cfg = PrefillTcCfg<D, NST, KV8, ALONE>;
   constexpr int NG = Cfg::NG;
   constexpr int NSS = Cfg::NSS > 0 ? Cfg::NSS : 1;
+  constexpr int kTcKeys = Cfg::KEYS, kTcPages = Cfg::PAGES, NSB = Cfg::NSB;
   extern __shared__ uint8_t smem_raw[];
   // per ring stage: K (or V) tile ready, K (or V) tile read
   __shared__ uint64_t full_k[NST], empty_k[NST], full_v[NST], empty_v[NST];
@@ -211,7 +240,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
   uint8_t* pKV = basep + Cfg::Q_BYTES;
   uint8_t* pV = pKV + Cfg::RING_BYTES;
   uint8_t* pP = pV + Cfg::RING_BYTES;
-  uint8_t* pStg = pP + 2 * NG * Cfg::P_BYTES;          // KV8: K staging, then V staging
+  uint8_t* pStg = pP + NSB * NG * Cfg::P_BYTES;        // KV8: K staging, then V staging
 
   bool failed = false;                                  // a wait ran out: stop waiting
   auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -222,10 +251,12 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
     }
   };
 
-  // ---- producers: warp W_K streams K tiles and warp W_V V tiles, each through
-  // its own TMA ring, so a K stage is refilled as soon as its S product is
-  // done and V stages wait only on the P.V products. A producer's lanes look
-  // up the page rows 32 pages (8 tiles) at a time, one chunk ahead, so no
+  // ---- producers: warps W_K .. W_K + PK - 1 stream the K tiles and warps
+  // W_V .. W_V + PV - 1 the V tiles, each operand through its own TMA ring, so
+  // a K stage is refilled as soon as its S product is done and V stages wait
+  // only on the P.V products; of the np producers of an operand, producer pw
+  // loads boxes (16 rows x 128 B) pw, pw + np, .. of each tile. A producer's
+  // lanes look up the page rows 32 pages at a time, one chunk ahead, so no
   // block-table read waits in front of a TMA issue; lane 0 issues the loads.
   const int pg_begin = t_begin * kTcPages;
   const int pg_end = min(n_pages, (t_begin + n_tiles) * kTcPages);
@@ -239,7 +270,11 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
     return ((id * p.Hkv + h) << p.ppb_shift) + (lp & ((1 << p.ppb_shift) - 1));
   };
   static_assert(32 % kTcPages == 0, "a tile's pages lie in one chunk");
-  const bool k_warp = warp == Cfg::W_K;
+  const bool k_warp = warp >= Cfg::W_K && warp < Cfg::W_K + Cfg::PK;
+  const bool v_warp = warp >= Cfg::W_V && warp < Cfg::W_V + Cfg::PV;
+  const bool producer = k_warp || v_warp;
+  const int np = k_warp ? Cfg::PK : Cfg::PV;              // producers of this operand
+  const int pw = k_warp ? warp - Cfg::W_K : warp - Cfg::W_V;   // boxes pw, pw + np, ..
   const CUtensorMap* tmap = k_warp ? &tmK : &tmV;
   uint64_t* full_x = k_warp ? full_k : full_v;
   uint64_t* empty_x = k_warp ? empty_k : empty_v;
@@ -268,16 +303,15 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
       }
     } else {
       const int st = u % NST;
-      if (lane == 0) mbar_arrive_expect_tx(&full_x[st], npg * kBS * D * 2);
+      const int nbx = npg * Cfg::NBOX;                   // boxes (16 rows x 128 B) of the tile
+      const int mine = pw < nbx ? (nbx - pw + np - 1) / np : 0;
+      if (lane == 0) mbar_arrive_expect_tx(&full_x[st], mine * kBS * 128);
       uint8_t* dst = ring_x + st * Cfg::KV_BYTES;
-      for (int pg = 0; pg < npg; ++pg) {
+      for (int b = pw; b < nbx; b += np) {
+        const int pg = b / Cfg::NBOX, bx = b % Cfg::NBOX;
         const int z = __shfl_sync(0xffffffffu, z_cur, (u * kTcPages + pg) % 32);
-        if (lane == 0) {
-#pragma unroll
-          for (int bx = 0; bx < Cfg::NBOX; ++bx)
-            tma_load_3d(dst + bx * Cfg::KV_BOX + pg * (kBS * 128), tmap, &full_x[st], bx * 64, 0,
-                        z);
-        }
+        if (lane == 0)
+          tma_load_3d(dst + bx * Cfg::KV_BOX + pg * (kBS * 128), tmap, &full_x[st], bx * 64, 0, z);
       }
     }
   };
@@ -327,9 +361,9 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
       for (int s = 0; s < NST; ++s) {
-        mbar_init(&full_k[s], KV8 ? 32 : 1);            // KV8: the converting warp's lanes
+        mbar_init(&full_k[s], KV8 ? 32 : Cfg::PK);      // KV8: the converting warp's lanes
         mbar_init(&empty_k[s], 1);
-        mbar_init(&full_v[s], KV8 ? 32 : 1);
+        mbar_init(&full_v[s], KV8 ? 32 : Cfg::PV);
         mbar_init(&empty_v[s], 1);
       }
       for (int s = 0; s < NSS; ++s) {
@@ -348,7 +382,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
     }
     __syncwarp();
   }
-  if (warp == Cfg::W_K || warp == Cfg::W_V) {
+  if (producer) {
     z_cur = page_row(pg_begin + lane);
     z_next = page_row(pg_begin + 32 + lane);
   }
@@ -405,86 +439,95 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
   if constexpr (SPLIT > 1) cluster_arrive();
   tc::fence_after();
   const uint32_t tm = tmem_base;
-  // TMEM columns: S of group g, buffer b at 64 (2g + b); O of group g at 128 NG + g D
+  // TMEM columns: S of group g, buffer b at KEYS (NSB g + b); O of group g after them
   const uint32_t tS = tm;
-  const uint32_t tO = tm + 2 * NG * kTcKeys;
+  const uint32_t tO = tm + NSB * NG * kTcKeys;
 
-  if (warp == Cfg::W_K || warp == Cfg::W_V) {
-    // the V producer starts once the barriers are set up (after the CTA barrier)
-    if constexpr (KV8) {
-      if (!k_warp)
-        for (int u = 0; u < Cfg::NSS && u < n_tiles; ++u) issue(u);
-      for (int u = 0; u < n_tiles; ++u) convert(u);
-    } else {
-      for (int u = k_warp ? NST : 0; u < n_tiles; ++u) {
-        if (u >= NST) wait(&empty_x[u % NST], ((u / NST) - 1) & 1);
-        issue(u);
-      }
+  // ---- producer and MMA warps (warpgroups 2 and 3 when registers move) ----------------
+  if (warp >= Cfg::W_K) {
+    if constexpr (Cfg::REALLOC) {
+      if (warp >= Cfg::W_MMA) tc::reg_lower<Cfg::REG_MV>();
+      else tc::reg_lower<Cfg::REG_K>();
     }
-    __syncwarp();
-    if constexpr (SPLIT > 1) cluster_wait();
-    return;
-  }
-
-  constexpr uint32_t ID_S = tc::idesc_f16(kTcRows, kTcKeys, BF16, false);
-  constexpr uint32_t ID_O = tc::idesc_f16(kTcRows, D, BF16, true);
-
-  // Tile u belongs to group g = u % NG as its j-th tile (j = u / NG): S goes to
-  // TMEM buffer (g, j % 2), P to shared buffer (g, j % 2), P.V accumulates
-  // into O of group g. Each barrier (g, b) completes once per use of its
-  // buffer, so every phase is waited on in order.
-  if (warp == Cfg::W_MMA) {
-    // ---- MMA warp: issues whatever is ready, S products first. S of tile u
-    // needs its K tile landed and its TMEM buffer free: the buffer's previous
-    // tile is u - 2 NG, whose softmax finished reading it before writing the P
-    // that the P.V of u - 2 NG waited for, so S may run up to 2 NG tiles ahead
-    // of the P.V products. P.V of tile u (in order) needs the group's P. -------
-    if (lane == 0) {
-      int us = 0, up = 0;                               // next S, next P.V
-      uint32_t idle = 0;
-      while (up < n_tiles && !failed) {
-        if (us < n_tiles && us < up + 2 * NG &&
-            mbar_test_wait(&full_k[us % NST], (us / NST) & 1)) {
-          const int g = us % NG, j = us / NG;
-          tc::fence_after();
-          const uint32_t kst = sKV + (us % NST) * Cfg::KV_BYTES;
-#pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t ko = (k % 4) * 32u;
-            const uint64_t a = tc::sdesc(sQ + (k / 4) * Cfg::Q_BOX + ko, 16, 1024);
-            const uint64_t bd = tc::sdesc(kst + (k / 4) * Cfg::KV_BOX + ko, 16, 1024);
-            tc::mma(tS + (2 * g + (j & 1)) * kTcKeys, a, bd, ID_S, k > 0 ? 1u : 0u);
-          }
-          tc::commit(&s_bar[g][j & 1]);
-          tc::commit(&empty_k[us % NST]);               // the K stage is free once S is done
-          ++us;
-          idle = 0;
-        } else if (up < us &&
-                   mbar_test_wait(&p_bar[up % NG][(up / NG) & 1], ((up / NG) >> 1) & 1) &&
-                   mbar_test_wait(&full_v[up % NST], (up / NST) & 1)) {
-          const int g = up % NG, j = up / NG, b = j & 1;
-          tc::fence_after();
-          const uint32_t vst = sV + (up % NST) * Cfg::KV_BYTES;
-#pragma unroll
-          for (int k = 0; k < kTcKeys / 16; ++k) {
-            const uint64_t a = tc::sdesc(sP + (2 * g + b) * Cfg::P_BYTES + k * 32, 16, 1024);
-            const uint64_t bd = tc::sdesc(vst + k * 2 * 1024, Cfg::KV_BOX, 1024);
-            tc::mma(tO + g * D, a, bd, ID_O, (j > 0 || k > 0) ? 1u : 0u);
-          }
-          tc::commit(&o_bar[g][b]);
-          tc::commit(&empty_v[up % NST]);               // the V stage is free once P.V is done
-          ++up;
-          idle = 0;
-        } else if (++idle > (1u << 26)) {
-          failed = true;                                // nothing became ready: give up
-          atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+    if (producer) {
+      // the other producers start once the barriers are set up (after the CTA barrier)
+      if constexpr (KV8) {
+        if (!k_warp)
+          for (int u = 0; u < Cfg::NSS && u < n_tiles; ++u) issue(u);
+        for (int u = 0; u < n_tiles; ++u) convert(u);
+      } else {
+        for (int u = warp == Cfg::W_K ? NST : 0; u < n_tiles; ++u) {
+          if (u >= NST) wait(&empty_x[u % NST], ((u / NST) - 1) & 1);
+          issue(u);
         }
       }
+      __syncwarp();
+      if constexpr (SPLIT > 1) cluster_wait();
+      return;
     }
-    __syncwarp();
-    if constexpr (SPLIT > 1) cluster_wait();
-    return;
+
+    constexpr uint32_t ID_S = tc::idesc_f16(kTcRows, kTcKeys, BF16, false);
+    constexpr uint32_t ID_O = tc::idesc_f16(kTcRows, D, BF16, true);
+
+    // Tile u belongs to group g = u % NG as its j-th tile (j = u / NG): S goes to
+    // TMEM buffer (g, j % NSB), P to shared buffer (g, j % NSB), P.V accumulates
+    // into O of group g. Each barrier (g, b) completes once per use of its
+    // buffer (use j / NSB), so every phase is waited on in order.
+    if (warp == Cfg::W_MMA) {
+      // ---- MMA warp: issues whatever is ready, S products first. S of tile u
+      // needs its K tile landed and its TMEM buffer free: the buffer's previous
+      // tile is u - NSB NG, whose softmax finished reading it before writing the
+      // P that the P.V of u - NSB NG waited for, so S may run up to NSB NG tiles
+      // ahead of the P.V products. P.V of tile u (in order) needs the group's P.
+      if (lane == 0) {
+        int us = 0, up = 0;                               // next S, next P.V
+        uint32_t idle = 0;
+        while (up < n_tiles && !failed) {
+          if (us < n_tiles && us < up + NSB * NG &&
+              mbar_test_wait(&full_k[us % NST], (us / NST) & 1)) {
+            const int g = us % NG, j = us / NG;
+            tc::fence_after();
+            const uint32_t kst = sKV + (us % NST) * Cfg::KV_BYTES;
+  #pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t ko = (k % 4) * 32u;
+              const uint64_t a = tc::sdesc(sQ + (k / 4) * Cfg::Q_BOX + ko, 16, 1024);
+              const uint64_t bd = tc::sdesc(kst + (k / 4) * Cfg::KV_BOX + ko, 16, 1024);
+              tc::mma(tS + (NSB * g + j % NSB) * kTcKeys, a, bd, ID_S, k > 0 ? 1u : 0u);
+            }
+            tc::commit(&s_bar[g][j % NSB]);
+            tc::commit(&empty_k[us % NST]);               // the K stage is free once S is done
+            ++us;
+            idle = 0;
+          } else if (up < us &&
+                     mbar_test_wait(&p_bar[up % NG][(up / NG) % NSB], ((up / NG) / NSB) & 1) &&
+                     mbar_test_wait(&full_v[up % NST], (up / NST) & 1)) {
+            const int g = up % NG, j = up / NG, b = j % NSB;
+            tc::fence_after();
+            const uint32_t vst = sV + (up % NST) * Cfg::KV_BYTES;
+  #pragma unroll
+            for (int k = 0; k < kTcKeys / 16; ++k) {
+              const uint64_t a = tc::sdesc(
+                  sP + (NSB * g + b) * Cfg::P_BYTES + (k / 4) * Cfg::P_CB + (k % 4) * 32, 16, 1024);
+              const uint64_t bd = tc::sdesc(vst + k * 2 * 1024, Cfg::KV_BOX, 1024);
+              tc::mma(tO + g * D, a, bd, ID_O, (j > 0 || k > 0) ? 1u : 0u);
+            }
+            tc::commit(&o_bar[g][b]);
+            tc::commit(&empty_v[up % NST]);               // the V stage is free once P.V is done
+            ++up;
+            idle = 0;
+          } else if (++idle > (1u << 26)) {
+            failed = true;                                // nothing became ready: give up
+            atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+          }
+        }
+      }
+      __syncwarp();
+      if constexpr (SPLIT > 1) cluster_wait();
+      return;
+    }
   }
+  if constexpr (Cfg::REALLOC) tc::reg_raise<Cfg::REG_SOFTMAX>();
 
   // ---- warps 0 .. 4 NG - 1: the softmax groups, one row per thread each ------------
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -499,30 +542,40 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
     const int u = NG * j + grp;                         // local tile
     const int t = t_begin + u;                          // key tile
     const int st = u % NST;
-    const int b = j & 1;
-    wait(&s_bar[grp][b], (j >> 1) & 1);
+    const int b = j % NSB;
+    wait(&s_bar[grp][b], (j / NSB) & 1);
     tc::fence_after();
-    uint32_t sv[2][32];
-    const uint32_t sbuf = tS + (2 * grp + b) * kTcKeys + lane_base;
-    tc::ld32(sbuf, sv[0]);
-    tc::ld32(sbuf + 32, sv[1]);
-    tc::wait_ld();
-    // raw scores; keys past this row's causal limit become -inf (only the
-    // tiles that cross the limit need the test)
-    float x[kTcKeys];
+    const uint32_t sbuf = tS + (NSB * grp + b) * kTcKeys + lane_base;
+    // raw scores, 64 keys at a time; keys past this row's causal limit become
+    // -inf (only the halves that cross the limit need the test). A 128-key
+    // tile is read from TMEM twice, for the max and then for P, which keeps
+    // 64 scores in registers
+    constexpr int HALVES = kTcKeys / 64;
+    float x[64];
+    auto load_half = [&](int hh) {
+      uint32_t sv[2][32];
+      tc::ld32(sbuf + hh * 64, sv[0]);
+      tc::ld32(sbuf + hh * 64 + 32, sv[1]);
+      tc::wait_ld();
 #pragma unroll
-    for (int c = 0; c < kTcKeys; ++c) x[c] = __uint_as_float(sv[c / 32][c % 32]);
-    if (t * kTcKeys + kTcKeys - 1 > lim) {
+      for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sv[c / 32][c % 32]);
+      const int k0 = t * kTcKeys + hh * 64;
+      if (k0 + 63 > lim) {
 #pragma unroll
-      for (int c = 0; c < kTcKeys; ++c)
-        if (t * kTcKeys + c > lim) x[c] = -INFINITY;
-    }
+        for (int c = 0; c < 64; ++c)
+          if (k0 + c > lim) x[c] = -INFINITY;
+      }
+    };
     // row max over 8 independent chains, then a tree
     float m8[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) m8[k] = x[k];
+    for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
 #pragma unroll
-    for (int c = 8; c < kTcKeys; ++c) m8[c % 8] = fmaxf(m8[c % 8], x[c]);
+    for (int hh = 0; hh < HALVES; ++hh) {
+      load_half(hh);
+#pragma unroll
+      for (int c = 0; c < 64; ++c) m8[c % 8] = fmaxf(m8[c % 8], x[c]);
+    }
 #pragma unroll
     for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
@@ -534,7 +587,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
     if (move) m_ref = mx;
     if (j > 0 && __any_sync(0xffffffffu, move)) {
       // O must hold every earlier tile of this group before it is scaled
-      wait(&o_bar[grp][(j - 1) & 1], ((j - 1) >> 1) & 1);
+      wait(&o_bar[grp][(j - 1) % NSB], ((j - 1) / NSB) & 1);
       tc::fence_after();
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
@@ -547,24 +600,28 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
       }
       tc::wait_st();
     }
-    // P buffer b was read by the P.V of this group's tile j - 2
-    if (j >= 2) wait(&o_bar[grp][b], ((j - 2) >> 1) & 1);
+    // P buffer b was read by the P.V of this group's tile j - NSB
+    if (j >= NSB) wait(&o_bar[grp][b], ((j - NSB) / NSB) & 1);
     const float ms = m_ref == -INFINITY ? 0.f : m_ref;
-    uint8_t* pPb = pP + (2 * grp + b) * Cfg::P_BYTES;
+    uint8_t* pPb = pP + (NSB * grp + b) * Cfg::P_BYTES;
     float rs8[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) rs8[k] = 0.f;
 #pragma unroll
-    for (int c = 0; c < kTcKeys / 8; ++c) {
-      float e[8];
+    for (int hh = 0; hh < HALVES; ++hh) {
+      if (HALVES > 1) load_half(hh);                    // (one half: x still holds it)
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        e[k] = ex2_approx(fmaf(x[8 * c + k], sl2, -ms));
-        rs8[k] += e[k];
+      for (int c = 0; c < 8; ++c) {
+        float e[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          e[k] = ex2_approx(fmaf(x[8 * c + k], sl2, -ms));
+          rs8[k] += e[k];
+        }
+        const uint4 w = make_uint4(pack16x2<BF16>(e[0], e[1]), pack16x2<BF16>(e[2], e[3]),
+                                   pack16x2<BF16>(e[4], e[5]), pack16x2<BF16>(e[6], e[7]));
+        *reinterpret_cast<uint4*>(pPb + hh * Cfg::P_CB + swz128(r, c)) = w;
       }
-      const uint4 w = make_uint4(pack16x2<BF16>(e[0], e[1]), pack16x2<BF16>(e[2], e[3]),
-                                 pack16x2<BF16>(e[4], e[5]), pack16x2<BF16>(e[6], e[7]));
-      *reinterpret_cast<uint4*>(pPb + swz128(r, c)) = w;
     }
 #pragma unroll
     for (int w = 4; w > 0; w >>= 1)
@@ -595,17 +652,17 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
   if (n_mine > 0) {
     // MMAs complete in issue order: this group's last P.V done means all of its are
     const int jl = n_mine - 1;
-    wait(&o_bar[grp][jl & 1], (jl >> 1) & 1);
+    wait(&o_bar[grp][jl % NSB], (jl / NSB) & 1);
     tc::fence_after();
   }
   // The groups' shares of row r: O_g relative to 2^m_g with sum l_g.
   // Combined: M = max(m_0, m_1), O = O_0 w_0 + O_1 w_1 with w_g = 2^(m_g - M),
   // and the same for the sum. (reference max, sum) of each row go through the
   // group's first P buffer, which its last P.V has finished reading.
-  reinterpret_cast<float2*>(pP + 2 * grp * Cfg::P_BYTES)[r] = make_float2(m_ref, l);
+  reinterpret_cast<float2*>(pP + NSB * grp * Cfg::P_BYTES)[r] = make_float2(m_ref, l);
   named_barrier(1, NG * kTcRows);
   const float2 ml0 = reinterpret_cast<const float2*>(pP)[r];
-  const float2 ml1 = NG > 1 ? reinterpret_cast<const float2*>(pP + 2 * Cfg::P_BYTES)[r]
+  const float2 ml1 = NG > 1 ? reinterpret_cast<const float2*>(pP + NSB * Cfg::P_BYTES)[r]
                             : make_float2(-INFINITY, 0.f);
   // a group with no tile has no O
   const bool has0 = n_tiles > 0, has1 = NG > 1 && n_tiles > 1;
@@ -702,21 +759,29 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3>::THREADS, 
   if (warp == 0) tc::dealloc(tm, Cfg::TMEM_COLS);
 }
 
-template <int D, int KV, bool QBF16, int SPLIT>
+template <int D, int KV, bool QBF16, int SPLIT, bool ALONE>
 static pkv_status launch_prefill_tc_s(const PrefillParams& q, const CUtensorMap& tmK,
                                       const CUtensorMap& tmV, cudaStream_t stream, int dev) {
   constexpr bool KV8 = KV == KV_E4M3;
-  constexpr int NST = (D > 128 || KV8) ? 2 : 4;
-  using Cfg = PrefillTcCfg<D, NST, KV8>;
+  // ring stages: 2 for the 128-key tiles at D = 128 (32 KB each), for E4M3 and D = 256
+  constexpr int NST = (D > 128 || KV8 || (ALONE && D == 128)) ? 2 : 4;
+  using Cfg = PrefillTcCfg<D, NST, KV8, ALONE>;
   static_assert(Cfg::SMEM_BYTES + 512 <= 227 * 1024, "shared memory (dynamic + static)");
   static_assert(SPLIT == 1 || kTcRows * (D / SPLIT) * 4 + kTcRows * 8 <= 2 * Cfg::RING_BYTES,
                 "the other CTA's rows must fit in the ring");
-  auto kern = prefill_tc_kernel<D, KV, QBF16, NST, SPLIT>;
+  auto kern = prefill_tc_kernel<D, KV, QBF16, NST, SPLIT, ALONE>;
   static std::atomic<bool> attr_set[64];  // per device; the call is idempotent
   if (!attr_set[dev]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg::SMEM_BYTES) != cudaSuccess)
       return PKV_ERR_CUDA;
+    if constexpr (Cfg::REALLOC) {
+      // a register raise waits for registers the CTA does not have unless
+      // the launch allocation covers every warpgroup's count: never launch then
+      cudaFuncAttributes fa{};
+      if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return PKV_ERR_CUDA;
+      if ((int64_t)fa.numRegs * Cfg::THREADS < Cfg::REG_TOTAL) return PKV_ERR_UNSUPPORTED;
+    }
     attr_set[dev] = true;
   }
   const int tiles = (q.max_q_len + q.q_tile - 1) / q.q_tile;
@@ -737,7 +802,7 @@ static pkv_status launch_prefill_tc_s(const PrefillParams& q, const CUtensorMap&
 
 // One CTA per query tile when that fills at least half of the GPU (or other
 // work shares it); otherwise a cluster of two per tile, each taking half of
-// the key tiles.
+// the key tiles. Beside a decode grid (may_split false), the 64-key tiles.
 template <int D, int KV, bool QBF16>
 static pkv_status launch_prefill_tc_t(const PrefillParams& p, const CUtensorMap& tmK,
                                       const CUtensorMap& tmV, cudaStream_t stream,
@@ -754,9 +819,10 @@ static pkv_status launch_prefill_tc_t(const PrefillParams& p, const CUtensorMap&
   PrefillParams q = p;
   q.q_tile = kTcRows / p.G;
   const int64_t ctas = (int64_t)((q.max_q_len + q.q_tile - 1) / q.q_tile) * q.Hkv * q.num_seqs;
-  if (may_split && 2 * ctas <= n_sms)
-    return launch_prefill_tc_s<D, KV, QBF16, 2>(q, tmK, tmV, stream, dev);
-  return launch_prefill_tc_s<D, KV, QBF16, 1>(q, tmK, tmV, stream, dev);
+  if (!may_split) return launch_prefill_tc_s<D, KV, QBF16, 1, false>(q, tmK, tmV, stream, dev);
+  if (2 * ctas <= n_sms)
+    return launch_prefill_tc_s<D, KV, QBF16, 2, true>(q, tmK, tmV, stream, dev);
+  return launch_prefill_tc_s<D, KV, QBF16, 1, true>(q, tmK, tmV, stream, dev);
 }
 
 template <int D>

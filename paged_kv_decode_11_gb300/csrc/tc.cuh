@@ -127,5 +127,19 @@ __device__ __forceinline__ void wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Registers per thread of the calling warpgroup, raised to / lowered to N
+// (every warp of the warpgroup executes the same call). A raise waits until
+// other warpgroups of the CTA have released enough of the registers the CTA
+// was launched with, so the counts of all warpgroups must add up to at most
+// that launch total.
+template <int N>
+__device__ __forceinline__ void reg_raise() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void reg_lower() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 }  // namespace tc
 }  // namespace pkv
