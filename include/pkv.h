@@ -286,11 +286,17 @@ pkv_status paged_attn_prefill_chunk(void* out, const void* q,
  *   [total_q_tokens, Hq]. block_tables [num_seqs, max_blocks_per_seq] and
  *   seq_lens [num_seqs] as for decode and prefill (seq_lens include the new
  *   tokens, already cached by reshape_and_cache).
- *   Decode rows are computed exactly as paged_attn_decode computes them
- *   (max_decode_seq_len bounds their seq_lens and sizes the split; the
- *   workspace is paged_attn_decode_workspace_size(num_decode_seqs, Hq, Hkv,
- *   D, max_decode_seq_len, partition_tokens) bytes), chunk rows exactly as
- *   paged_attn_prefill_chunk computes them (max_q_len bounds every chunk).
+ *   Decode rows are computed by paged_attn_decode's kernel (max_decode_seq_len
+ *   bounds their seq_lens and sizes the split; the workspace is
+ *   paged_attn_decode_workspace_size(num_decode_seqs, Hq, Hkv, D,
+ *   max_decode_seq_len, partition_tokens) bytes). With an explicit
+ *   partition_tokens they equal a separate paged_attn_decode call bit for
+ *   bit; with partition_tokens = 0 and chunks in the call, the automatic
+ *   partitions are sized for one resident decode CTA per SM (the prefill
+ *   grid holds SMs meanwhile), so they may round differently from a
+ *   separate call. Chunk rows are the causal attention of
+ *   paged_attn_prefill_chunk (max_q_len bounds every chunk); a chunk call of
+ *   its own may use other tile shapes and sum in another order.
  *   Everything is enqueued on `stream`: the prefill kernel, then the decode
  *   kernel launched as a programmatic dependent of the prefill kernel, so
  *   decode CTAs start on the room the prefill grid leaves instead of

@@ -181,7 +181,8 @@ pkv_status decode_setup(void* out, const void* q, pkv_dtype q_dtype, const void*
                         int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
                         int max_seq_len, float scale, const float* k_scales,
                         const float* v_scales, int partition_tokens, float* out_lse,
-                        void* workspace, size_t workspace_bytes, DecodeCall* call) {
+                        void* workspace, size_t workspace_bytes, DecodeCall* call,
+                        int plan_ctas_per_sm = kDecodeWorkers) {
   call->empty = true;
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_seq_len < 0 ||
       max_blocks_per_seq <= 0 || num_blocks <= 0 || partition_tokens < 0)
@@ -213,7 +214,7 @@ pkv_status decode_setup(void* out, const void* q, pkv_dtype q_dtype, const void*
 
   const int sms = sm_count();
   const DecodePlan pl = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len,
-                                    partition_tokens, sms);
+                                    partition_tokens, sms, plan_ctas_per_sm);
   if (workspace == nullptr || workspace_bytes < pl.bytes ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return PKV_ERR_WORKSPACE;
@@ -449,11 +450,15 @@ pkv_status paged_attn_varlen(void* out, const void* q, pkv_dtype q_dtype, const 
                                           : nullptr;
   DecodeCall dc;
   PrefillCall pc;
+  // with chunks in the call, the prefill grid holds SMs while decode runs, and
+  // automatic decode partitions are planned for one resident CTA per SM
+  // (longer partitions: the mixed step 2-5 us faster; the same plan slowed a
+  // decode call that has the GPU to itself)
   pkv_status st = decode_setup(out, q, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
                                seq_lens, num_decode_seqs, num_q_heads, num_kv_heads, head_dim,
                                block_size, max_blocks_per_seq, num_blocks, max_decode_seq_len,
                                scale, k_scales, v_scales, partition_tokens, out_lse, workspace,
-                               workspace_bytes, &dc);
+                               workspace_bytes, &dc, n_pf > 0 ? 1 : kDecodeWorkers);
   if (st != PKV_OK) return st;
   // the chunks' query rows follow the decode rows; their offsets in
   // query_start_loc[num_decode_seqs ..] are absolute rows of q and out

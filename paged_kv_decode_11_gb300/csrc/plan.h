@@ -12,9 +12,11 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Split-KV plan of a decode call. With partition_tokens = 0 the partition
 // is the smallest power of two from 512 to 2048 tokens that keeps the launch
-// at about 3 waves of resident CTAs when contexts average half the maximum
-// (below 512 tokens a CTA's start and merge cost more than the extra
-// parallelism gives back); an explicit size is honoured as given.
+// at about 3 waves of ctas_per_sm resident CTAs on every SM when contexts
+// average half the maximum (below 512 tokens a CTA's start and merge cost
+// more than the extra parallelism gives back); an explicit size is honoured
+// as given. A larger ctas_per_sm never gives a longer partition, so the
+// workspace planned with the default fits every plan.
 // Workspace: [done counters B*Hkv u64 | partition outputs rows*D fp32 |
 // partition log2-sum-exps rows fp32], each region 256-byte aligned, with
 // rows = B * Hq * max_parts and max_parts = ceil(max_seq_len / partition).
@@ -24,14 +26,15 @@ struct DecodePlan {
 };
 
 inline DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                              int max_seq_len, int partition_tokens, int sms) {
+                              int max_seq_len, int partition_tokens, int sms,
+                              int ctas_per_sm = kDecodeWorkers) {
   DecodePlan pl{};
   if (sms <= 0) sms = 148;
   if (partition_tokens > 0) {
     pl.part = partition_tokens;
   } else {
     const int64_t est = (int64_t)num_seqs * num_kv_heads * std::max(1, max_seq_len / 2);
-    const int64_t target = (int64_t)sms * kDecodeWorkers * 3;
+    const int64_t target = (int64_t)sms * ctas_per_sm * 3;
     pl.part = 512;
     while (pl.part < 2048 && est / pl.part > target) pl.part *= 2;
   }
