@@ -64,6 +64,7 @@ __global__ void __launch_bounds__(NW * 32)
   __shared__ int s_ids[NIDS];
   __shared__ int s_last;
   __shared__ int s_stuck;         // a warp's copies may still land in the ring
+  __shared__ uint64_t s_mbar;     // the merge's bulk copies of the partials
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
@@ -131,6 +132,7 @@ __global__ void __launch_bounds__(NW * 32)
     for (int w = 0; w < NW; ++w)
 #pragma unroll
       for (int s = 0; s < NST; ++s) mbar_init(&bars[w][s], GATHER ? 32 : 1);
+    mbar_init(&s_mbar, 1);
     fence_barrier_init();
     s_stuck = 0;
   }
@@ -411,80 +413,88 @@ __global__ void __launch_bounds__(NW * 32)
   __syncthreads();
   if (!s_last) return;
   if (tid == 0) *ctr = 0ull;
-  // The warps split the partitions; each lane owns D/32 dims of every head.
-  // Pass 1: the largest log2-sum-exp of each head.
-  constexpr int PER = D / 32;
-  float* mbuf = red_m[0];                         // [G] maxima (G <= NH)
-  for (int hh = warp; hh < G; hh += NW) {
-    const float* lse = p.ws_lse + (row0 + hh) * p.max_parts;
-    float mx = -INFINITY;
-    for (int s2 = lane; s2 < nparts; s2 += 32) mx = fmaxf(mx, ldcg_f32(lse + s2));
+  // The CTA partials of (b, h) come into shared memory (the ring's space) in
+  // chunks of CH partitions. A head's partitions are consecutive rows of the
+  // workspace, so a chunk is one bulk copy per head plus the chunk's
+  // log2-sum-exps, all in flight before a single wait: one round trip per
+  // chunk, however many partitions it holds. Each thread then owns float4
+  // columns f = tid, tid + NW*32, ... of the G x D outputs and folds the
+  // chunk's partitions into a running log-sum-exp (max M, sum Z, weighted
+  // sum acc), rescaling when a partition's log2-sum-exp exceeds M.
+  constexpr int NTH = NW * 32;
+  constexpr int NF = (NH * (D / 4) + NTH - 1) / NTH;   // float4 columns per thread
+  constexpr int AVAIL = Cfg::SMEM_BYTES - 1024;         // the ring's space
+  const int CH = max(1, min(nparts, (AVAIL - 16) / (G * (D + 1) * 4)));
+  float* s_lse = reinterpret_cast<float*>(basep);                       // [G][CH]
+  float* s_o = reinterpret_cast<float*>(basep + ((G * CH * 4 + 15) & ~15));  // [G][CH][D]
+  float M[NF], Z[NF];
+  float4 acc[NF];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) mbuf[hh] = mx;
+  for (int i = 0; i < NF; ++i) {
+    M[i] = -INFINITY;
+    Z[i] = 0.f;
+    acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  __syncthreads();
-  // Pass 2: weighted sums, four heads at a time, partitions round-robin over warps.
-  for (int h0 = 0; h0 < G; h0 += 4) {
-    const int nh = min(4, G - h0);
-    float acc[4][PER], z[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      z[j] = 0.f;
-#pragma unroll
-      for (int i = 0; i < PER; ++i) acc[j][i] = 0.f;
+  const float* lse_rows = p.ws_lse + row0 * (int64_t)p.max_parts;
+  for (int c0 = 0, ci = 0; c0 < nparts; c0 += CH, ++ci) {
+    const int n = min(CH, nparts - c0);
+    if (tid == 0) {
+      // the partials were written through the generic proxy; the acquire
+      // above ordered them before this thread's reads, and this fence before
+      // its bulk copies
+      fence_proxy_async_global();
+      mbar_arrive_expect_tx(&s_mbar, (uint32_t)(G * n * D * 4));
+      for (int hh = 0; hh < G; ++hh)
+        bulk_load(s_o + hh * CH * D, p.ws_o + ((row0 + hh) * p.max_parts + c0) * D,
+                  (uint32_t)(n * D * 4), &s_mbar);
     }
 #pragma unroll 4
-    for (int s2 = warp; s2 < nparts; s2 += NW) {
+    for (int i = tid; i < G * n; i += NTH) {
+      const int hh = i / n, sp = i - hh * n;
+      s_lse[hh * CH + sp] = ldcg_f32(lse_rows + hh * p.max_parts + c0 + sp);
+    }
+    __syncthreads();
+    if (!mbar_wait_bounded(&s_mbar, ci & 1)) {
+      // leave only once the copies have landed (bounded): they target this
+      // CTA's shared memory
+      if (tid == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
+      mbar_wait_bounded(&s_mbar, ci & 1);
+      return;
+    }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (j >= nh) continue;
-        const int64_t wrow = (row0 + h0 + j) * p.max_parts + s2;
-        const float M = mbuf[h0 + j];
-        const float ls = ldcg_f32(p.ws_lse + wrow);
-        const float w = (ls == -INFINITY || M == -INFINITY) ? 0.f : exp2f(ls - M);
-        z[j] += w;
-        const float* o = p.ws_o + wrow * D + lane * PER;
-        if constexpr (PER % 4 == 0) {
-#pragma unroll
-          for (int v4 = 0; v4 < PER / 4; ++v4) {
-            const float4 v = __ldcg(reinterpret_cast<const float4*>(o) + v4);
-            acc[j][4 * v4] += w * v.x;
-            acc[j][4 * v4 + 1] += w * v.y;
-            acc[j][4 * v4 + 2] += w * v.z;
-            acc[j][4 * v4 + 3] += w * v.w;
+    for (int i = 0; i < NF; ++i) {
+      const int f = tid + i * NTH;
+      if (f < G * (D / 4)) {
+        const int hh = f / (D / 4), d4 = f - hh * (D / 4);
+        for (int sp = 0; sp < n; ++sp) {
+          const float ls = s_lse[hh * CH + sp];
+          if (ls == -INFINITY) continue;
+          if (ls > M[i]) {
+            const float sc = M[i] == -INFINITY ? 0.f : exp2f(M[i] - ls);
+            acc[i].x *= sc; acc[i].y *= sc; acc[i].z *= sc; acc[i].w *= sc;
+            Z[i] *= sc;
+            M[i] = ls;
           }
-        } else {
-          const float2 v = __ldcg(reinterpret_cast<const float2*>(o));
-          acc[j][0] += w * v.x; acc[j][1] += w * v.y;
+          const float w = exp2f(ls - M[i]);
+          const float4 v = *reinterpret_cast<const float4*>(s_o + (hh * CH + sp) * D + d4 * 4);
+          Z[i] += w;
+          acc[i].x += w * v.x; acc[i].y += w * v.y; acc[i].z += w * v.z; acc[i].w += w * v.w;
         }
       }
     }
-    // combine the warps through shared memory (the ring's space is free)
-    __syncthreads();
+    __syncthreads();   // the next chunk reuses the staging space
+  }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (j >= nh) break;
-#pragma unroll
-      for (int i = 0; i < PER; ++i) obuf[(warp * 4 + j) * D + lane * PER + i] = acc[j][i];
-      if (lane == 0) red_l[warp][j] = z[j];
-    }
-    __syncthreads();
-    for (int idx = tid; idx < nh * (D / 2); idx += NW * 32) {
-      const int j = idx / (D / 2), d = 2 * (idx % (D / 2));
-      float Z = 0.f, o0 = 0.f, o1 = 0.f;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        Z += red_l[w][j];
-        o0 += obuf[(w * 4 + j) * D + d];
-        o1 += obuf[(w * 4 + j) * D + d + 1];
-      }
-      const float inv = Z > 0.f ? vscale / Z : 0.f;
-      const int hh = h0 + j;
-      *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(p.out) + (row0 + hh) * D + d) =
-          pack2<QBF16>(o0 * inv, o1 * inv);
-      if (d == 0 && p.out_lse != nullptr)
-        p.out_lse[row0 + hh] = Z > 0.f ? (mbuf[hh] + log2f(Z)) * kLn2 : -INFINITY;
+  for (int i = 0; i < NF; ++i) {
+    const int f = tid + i * NTH;
+    if (f < G * (D / 4)) {
+      const int hh = f / (D / 4), d4 = f - hh * (D / 4);
+      const float inv = Z[i] > 0.f ? vscale / Z[i] : 0.f;
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + (row0 + hh) * D + d4 * 4) =
+          make_uint2(pack2<QBF16>(acc[i].x * inv, acc[i].y * inv),
+                     pack2<QBF16>(acc[i].z * inv, acc[i].w * inv));
+      if (d4 == 0 && p.out_lse != nullptr)
+        p.out_lse[row0 + hh] = Z[i] > 0.f ? (M[i] + log2f(Z[i])) * kLn2 : -INFINITY;
     }
   }
 }

@@ -266,6 +266,12 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 
 __device__ __forceinline__ float ldcg_f32(const float* p) { return __ldcg(p); }
 
+// Orders this thread's earlier generic-proxy view of global memory before its
+// later async-proxy (bulk copy) accesses of it.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Atomic add at GPU scope with acquire and release semantics; returns the old
 // value. Issued by one thread right after a CTA barrier, the release makes the
 // whole CTA's earlier writes visible before the add (release is cumulative
