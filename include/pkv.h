@@ -125,7 +125,10 @@ size_t paged_attn_decode_workspace_size(int num_seqs, int num_q_heads,
  *   Each context is cut into partitions (of `partition_tokens` tokens, a
  *   multiple of 16 up to 8192, or 0 = automatic sizes); each partition is
  *   reduced with an online softmax and the partitions of a sequence are
- *   merged by log-sum-exp in the same kernel launch.
+ *   merged by log-sum-exp in the same kernel launch. With 0, a batch whose
+ *   (sequence, KV head) pairs fit one per SM may be planned as one partition
+ *   per context (on head_dim <= 128 with blocks of 16 tokens or more): the
+ *   same attention, summed in another order than a split plan.
  *   seq_lens[b] == 0 gives out = 0 and lse = -inf.
  *   max_seq_len: upper bound on every seq_lens[b] (sizes the plan); a larger
  *   seq_len sets PKV_DEVERR_SEQ_LEN and is clamped.

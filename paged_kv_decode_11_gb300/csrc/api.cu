@@ -258,6 +258,9 @@ pkv_status decode_setup(void* out, const void* q, pkv_dtype q_dtype, const void*
   p.max_parts = pl.max_parts;
   p.wpart = warp_partition_tokens(partition_tokens, bs_log2);
   if (p.wpart > 0) p.part = p.wpart * kDecodeWarps;
+  p.wide = wide_decode((int64_t)num_seqs * num_kv_heads, sms, max_seq_len, partition_tokens,
+                       bs_log2, head_dim, plan_ctas_per_sm) ? 1 : 0;
+  if (p.wide) p.part = std::max(16, (max_seq_len + 15) / 16 * 16);   // one partition
   p.grid_parts = std::max(1, (max_seq_len + p.part - 1) / p.part);
   p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   p.wait_prior = 1;

@@ -2,7 +2,8 @@
 // log-sum-exp merge in one kernel launch, one CTA per (CTA partition, KV
 // head, sequence) (decode_kernel.cuh; the hardware hands CTAs to SMs as they
 // free up, which balances uneven SMs for free). Blocks of fewer than 16
-// tokens go to the gather instantiation in decode_gather.cu.
+// tokens go to the gather instantiation in decode_gather.cu, whole-context
+// plans to the 8-warp instantiation in decode_wide.cu.
 #include "decode_kernel.cuh"
 
 namespace pkv {
@@ -12,6 +13,8 @@ pkv_status launch_decode(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                          cudaStream_t stream, bool programmatic) {
   if (p.bs_log2 < 4)
     return launch_decode_gather(p, head_dim, q_dtype, kv_dtype, stream, programmatic);
+  if (p.wide)
+    return launch_decode_wide(p, head_dim, q_dtype, kv_dtype, tmK, tmV, stream, programmatic);
   return launch_decode_mode<false>(p, head_dim, q_dtype, kv_dtype, tmK, tmV, stream,
                                    programmatic);
 }

@@ -499,24 +499,22 @@ __global__ void __launch_bounds__(NW * 32)
   }
 }
 
-// Warps per CTA and TMA ring depth per warp (E4M3 / 16-bit caches).
-#ifndef PKV_DECODE_NW
-#define PKV_DECODE_NW 4
-#endif
-#ifndef PKV_DECODE_NST_E4M3
-#define PKV_DECODE_NST_E4M3 3
-#endif
-#ifndef PKV_DECODE_NST_16
-#define PKV_DECODE_NST_16 2
-#endif
+// TMA ring depth per warp: CTAs of kDecodeWarps warps (several resident per
+// SM) keep 3 stages of E4M3 pages or 2 of 16-bit pages; whole-context CTAs of
+// kDecodeWideWarps warps (an SM each) keep 3 of either.
+template <int NW, int KV>
+constexpr int decode_ring_stages() {
+  return NW == kDecodeWideWarps ? 3 : (KV == KV_E4M3 ? 3 : 2);
+}
 
-template <bool GATHER, int D, int KV, bool QBF16, int NT>
+template <bool GATHER, int D, int KV, bool QBF16, int NT, int NW>
 static pkv_status launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK,
                                   const CUtensorMap& tmV, cudaStream_t stream,
                                   bool programmatic) {
-  constexpr int NW = PKV_DECODE_NW;
-  constexpr int NST = (KV == KV_E4M3) ? PKV_DECODE_NST_E4M3 : PKV_DECODE_NST_16;
-  static_assert(NW == kDecodeWarps, "warp partitions are planned for kDecodeWarps warps");
+  constexpr int NST = decode_ring_stages<NW, KV>();
+  // warp partitions (p.wpart > 0) are planned for kDecodeWarps warps only
+  static_assert(NW == kDecodeWarps || (NW == kDecodeWideWarps && !GATHER),
+                "decode CTAs have kDecodeWarps warps, or kDecodeWideWarps with TMA pages");
   using Cfg = DecodeCfg<D, KV, NT, NW, NST>;
   auto kern = decode_kernel<D, KV, QBF16, NT, NW, NST, GATHER>;
   int dev = 0;
@@ -548,42 +546,43 @@ static pkv_status launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK,
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-template <bool GATHER, int D, int KV, bool QBF16>
+template <bool GATHER, int D, int KV, bool QBF16, int NW>
 static pkv_status launch_decode_nt(const DecodeParams& p, const CUtensorMap& tmK,
                                    const CUtensorMap& tmV, cudaStream_t stream, bool prog) {
   if constexpr (D <= 128) {
-    if (p.G > 8) return launch_decode_t<GATHER, D, KV, QBF16, 2>(p, tmK, tmV, stream, prog);
+    if (p.G > 8) return launch_decode_t<GATHER, D, KV, QBF16, 2, NW>(p, tmK, tmV, stream, prog);
   } else {
     if (p.G > 8) return PKV_ERR_UNSUPPORTED;        // 16 head columns at D = 256: not built
   }
-  return launch_decode_t<GATHER, D, KV, QBF16, 1>(p, tmK, tmV, stream, prog);
+  return launch_decode_t<GATHER, D, KV, QBF16, 1, NW>(p, tmK, tmV, stream, prog);
 }
 
-template <bool GATHER, int D>
+template <bool GATHER, int D, int NW>
 static pkv_status launch_decode_d(const DecodeParams& p, pkv_dtype q_dtype, pkv_dtype kv_dtype,
                                   const CUtensorMap& tmK, const CUtensorMap& tmV,
                                   cudaStream_t stream, bool prog) {
   const bool qbf = (q_dtype == PKV_BF16);
   if (kv_dtype == PKV_FP8_E4M3)
-    return qbf ? launch_decode_nt<GATHER, D, KV_E4M3, true>(p, tmK, tmV, stream, prog)
-               : launch_decode_nt<GATHER, D, KV_E4M3, false>(p, tmK, tmV, stream, prog);
+    return qbf ? launch_decode_nt<GATHER, D, KV_E4M3, true, NW>(p, tmK, tmV, stream, prog)
+               : launch_decode_nt<GATHER, D, KV_E4M3, false, NW>(p, tmK, tmV, stream, prog);
   if (kv_dtype == PKV_BF16)
-    return launch_decode_nt<GATHER, D, KV_BF16, true>(p, tmK, tmV, stream, prog);
-  return launch_decode_nt<GATHER, D, KV_F16, false>(p, tmK, tmV, stream, prog);
+    return launch_decode_nt<GATHER, D, KV_BF16, true, NW>(p, tmK, tmV, stream, prog);
+  return launch_decode_nt<GATHER, D, KV_F16, false, NW>(p, tmK, tmV, stream, prog);
 }
 
-template <bool GATHER>
+template <bool GATHER, int NW = kDecodeWarps>
 pkv_status launch_decode_mode(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                               pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
                               cudaStream_t stream, bool prog) {
-  if constexpr (GATHER) {
-    if (head_dim == 256) return PKV_ERR_UNSUPPORTED;   // rows too wide for the gather path
+  if constexpr (GATHER || NW == kDecodeWideWarps) {
+    // rows too wide for the gather path; rings too large for a wide CTA
+    if (head_dim == 256) return PKV_ERR_UNSUPPORTED;
   } else {
     if (head_dim == 256)
-      return launch_decode_d<GATHER, 256>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);
+      return launch_decode_d<GATHER, 256, NW>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);
   }
   if (head_dim == 128)
-    return launch_decode_d<GATHER, 128>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);
-  return launch_decode_d<GATHER, 64>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);
+    return launch_decode_d<GATHER, 128, NW>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);
+  return launch_decode_d<GATHER, 64, NW>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);
 }
 }  // namespace pkv

@@ -15,6 +15,7 @@ constexpr int kMaxPartitionTokens = 8192;
 constexpr int kGatherMaxPartitionTokens = 2048;   // split-KV partition cap (block ids staged in smem)
 constexpr int kDecodeWorkers = 4;           // resident decode CTAs per SM assumed by the planner
 constexpr int kDecodeWarps = 4;             // warps per decode CTA
+constexpr int kDecodeWideWarps = 8;         // warps per whole-context decode CTA
 
 struct DecodeParams {
   void* out;
@@ -38,6 +39,7 @@ struct DecodeParams {
                               // this many tokens (part = warps * wpart); 0: the warps
                               // take the CTA partition's pages round-robin
   int grid_parts;             // CTAs per (sequence, KV head) in the grid
+  int wide;                   // (host routing) whole-context CTAs of kDecodeWideWarps warps
   float qk_scale_log2;        // scale * log2(e)
   int wait_prior;             // wait for the grids ahead of it on the stream before reading
   // early start (per-partition kernel, TMA pages): the kernel ahead of it is
@@ -99,6 +101,11 @@ struct RopeCacheParams {
 pkv_status launch_decode(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                          pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
                          cudaStream_t stream, bool programmatic = false);
+// Whole-context decode (p.wide): one CTA of kDecodeWideWarps warps per
+// (sequence, KV head), head_dim 64 or 128, pages loaded by TMA.
+pkv_status launch_decode_wide(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
+                              pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                              cudaStream_t stream, bool programmatic);
 // Decode for blocks of fewer than 16 tokens (pages gathered row by row).
 pkv_status launch_decode_gather(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                                 pkv_dtype kv_dtype, cudaStream_t stream, bool programmatic);

@@ -48,6 +48,26 @@ inline DecodePlan plan_decode(int num_seqs, int num_q_heads, int num_kv_heads, i
   return pl;
 }
 
+// Whole-context decode: one CTA of kDecodeWideWarps warps per (sequence, KV
+// head), its context one partition (no workspace partials, no cross-CTA
+// merge), each warp keeping a deeper ring of pages in flight; the CTA takes an
+// SM to itself. It pays when that grid is about one full wave: automatic
+// partitions, pages loaded by TMA, head_dim <= 128, no other grid beside it
+// (ctas_per_sm at the default), (sequence, KV head) units at most one per SM,
+// and either short contexts (<= 512 tokens, where the split plan has one
+// partition anyway and the extra warps shorten each warp's chain of pages) or
+// at least 3/4 of the SMs busy with contexts of at most 4096 tokens (the
+// longest context bounds the call, at one CTA's rate). The workspace the
+// split plan sizes is always enough (this plan needs none of it).
+inline bool wide_decode(int64_t units, int sms, int max_seq_len, int partition_tokens,
+                        int bs_log2, int head_dim, int ctas_per_sm) {
+  if (partition_tokens > 0 || bs_log2 < 4 || head_dim > 128 || ctas_per_sm != kDecodeWorkers ||
+      sms <= 0 || units > sms)
+    return false;
+  if (max_seq_len <= 512) return true;
+  return max_seq_len <= 4096 && units * 4 >= (int64_t)sms * 3;
+}
+
 // Tokens of the partition each warp of a decode CTA reduces on its own, or 0.
 // With an explicit partition size (blocks of 16 tokens or more, pages loaded
 // by TMA) the kDecodeWarps warps of a CTA take consecutive partitions of one

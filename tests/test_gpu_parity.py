@@ -127,6 +127,24 @@ def test_decode_shape_sweep(D, Hq, Hkv, dtype, kv, part):
     _decode_vs_oracle(c, partition_tokens=part)
 
 
+@pytest.mark.parametrize("extra", [0, 1])
+@pytest.mark.parametrize("kv", ["same", "fp8"])
+def test_decode_automatic_plan_either_side_of_one_cta_per_sm(extra, kv):
+    # automatic partitions: with (sequence, KV head) units at most one per SM
+    # (and contexts up to 4096 tokens) the planner takes the whole-context
+    # 8-warp CTAs; one sequence more and it splits contexts into partitions
+    # merged across CTAs
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    Hkv = 8
+    B = sms // Hkv + extra
+    rng = np.random.default_rng(11)
+    ctx = [int(x) for x in rng.integers(1, 1500, size=B)]
+    ctx[:4] = [1, 16, 17, 1499]
+    c = make_case("tiny", 5, B=B, Hq=16, Hkv=Hkv, D=128, dtype="bf16", kv=kv,
+                  ctx=("fixed", ctx), pool=("scale", 1.25))
+    _decode_vs_oracle(c, partition_tokens=0)
+
+
 def test_decode_empty_sequences():
     c = make_case("tiny", 5, ctx=("fixed", [0, 40, 0, 1]))
     kc, vc = product_cache(c)
