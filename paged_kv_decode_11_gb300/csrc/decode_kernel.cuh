@@ -47,7 +47,106 @@ struct DecodeCfg {
       1024 + (RING_BYTES > OBUF_BYTES ? RING_BYTES : OBUF_BYTES);
 };
 
-template <int D, int KV, bool QBF16, int NT, int NW, int NST, bool GATHER>
+// Full-first CTA order (a 1-D grid of B * Hkv * grid_parts CTAs): CTA L
+// takes the L-th work item of a list that holds every full CTA partition
+// first (sequence by sequence, KV head, then partition), then each
+// sequence's last, shorter partition (and the single empty one of a
+// zero-length context) in order of decreasing length, ties by sequence. The
+// hardware hands out CTAs in index order as SMs free up, so this is a
+// longest-first schedule: the short partitions fill the final wave instead
+// of full ones starting late. Every CTA derives the list from seq_lens
+// (B <= kFullFirstMaxSeqs values, in the dynamic shared memory, free at this
+// point).
+// Returns false for CTAs past the list. Invalid seq_lens are clamped as in
+// the grid order, and CTA 0 flags them.
+template <int NW>
+__device__ bool decode_item_full_first(const DecodeParams& p, int cap, int* s_tmp, int& part_idx,
+                                       int& h, int& b, int& ctx) {
+  constexpr int NTH = NW * 32;
+  __shared__ int s_wsum[NW];
+  __shared__ int s_item[3];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int B = p.B, Hkv = p.Hkv, part = p.part;
+  const int L = blockIdx.x;
+  int* s_ctx = s_tmp;          // [B] clamped context lengths
+  int* s_last = s_tmp + B;     // [B] length of the last partial partition, -1 if none
+  bool bad = false;
+  for (int i = tid; i < B; i += NTH) {
+    int v = p.seq_lens[i];
+    if (v < 0 || v > cap) {
+      bad = true;
+      v = v < 0 ? 0 : cap;
+    }
+    s_ctx[i] = v;
+    s_last[i] = (v == 0) ? 0 : ((v % part) ? v % part : -1);
+  }
+  if (tid == 0) s_item[0] = -1;
+  if (__syncthreads_or(bad) && L == 0 && tid == 0) atomicOr(p.err, PKV_DEVERR_SEQ_LEN);
+  // exclusive scan of the full partitions over sequences (consecutive
+  // sequences per thread)
+  const int per = (B + NTH - 1) / NTH;
+  const int b_lo = min(B, tid * per), b_hi = min(B, b_lo + per);
+  int mine = 0;
+  for (int i = b_lo; i < b_hi; ++i) mine += s_ctx[i] / part;
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_wsum[warp] = incl;
+  __syncthreads();
+  int before = 0, nfull = 0;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    before += (w < warp) ? s_wsum[w] : 0;
+    nfull += s_wsum[w];
+  }
+  const int64_t full_items = (int64_t)Hkv * nfull;
+  if (L < full_items) {
+    int f = before + incl - mine;
+    for (int i = b_lo; i < b_hi; ++i) {
+      const int nf = s_ctx[i] / part;
+      const int64_t lo = (int64_t)Hkv * f;
+      if (L >= lo && L < lo + (int64_t)Hkv * nf) {
+        const int loc = (int)(L - lo);
+        s_item[0] = i;
+        s_item[1] = loc / nf;
+        s_item[2] = loc % nf;
+      }
+      f += nf;
+    }
+  } else {
+    const int64_t j = L - full_items;
+    const int r = (int)(j / Hkv), hh = (int)(j % Hkv);
+    if (r < B) {
+      for (int i = tid; i < B; i += NTH) {
+        const int li = s_last[i];
+        if (li < 0) continue;
+        int rank = 0;
+        for (int k = 0; k < B; ++k) {
+          const int lk = s_last[k];
+          rank += (lk > li) || (lk == li && k < i);
+        }
+        if (rank == r) {
+          s_item[0] = i;
+          s_item[1] = hh;
+          s_item[2] = s_ctx[i] / part;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  b = s_item[0];
+  if (b < 0) return false;
+  h = s_item[1];
+  part_idx = s_item[2];
+  ctx = s_ctx[b];
+  __syncthreads();   // the ring's space is reused from here on
+  return true;
+}
+
+template <int D, int KV, bool QBF16, int NT, int NW, int NST, bool GATHER, bool FF>
 __global__ void __launch_bounds__(NW * 32)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const DecodeParams p) {
@@ -68,7 +167,6 @@ __global__ void __launch_bounds__(NW * 32)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int part_idx = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int G = p.G;
   // launched as a programmatic dependent: the CTA is resident early, and
   // reads nothing before the kernel ahead of it (the cache write) is done;
@@ -76,11 +174,22 @@ __global__ void __launch_bounds__(NW * 32)
   const bool early = !GATHER && p.early != 0;
   if (p.wait_prior && !early) griddep_wait();
 
-  int ctx = p.seq_lens[b];
   const int cap = min(p.max_seq_len, p.max_blocks << p.bs_log2);
-  if (ctx < 0 || ctx > cap) {
-    if (tid == 0 && part_idx == 0 && h == 0) atomicOr(p.err, PKV_DEVERR_SEQ_LEN);
-    ctx = ctx < 0 ? 0 : cap;
+  int part_idx, h, b, ctx;
+  if constexpr (FF) {
+    // (the dynamic shared memory is free until the ring starts)
+    if (!decode_item_full_first<NW>(p, cap, reinterpret_cast<int*>(smem_raw), part_idx, h, b,
+                                    ctx))
+      return;
+  } else {
+    part_idx = blockIdx.x;
+    h = blockIdx.y;
+    b = blockIdx.z;
+    ctx = p.seq_lens[b];
+    if (ctx < 0 || ctx > cap) {
+      if (tid == 0 && part_idx == 0 && h == 0) atomicOr(p.err, PKV_DEVERR_SEQ_LEN);
+      ctx = ctx < 0 ? 0 : cap;
+    }
   }
   const int nparts = ctx > 0 ? (ctx + p.part - 1) / p.part : 1;
   if (part_idx >= nparts) return;
@@ -507,7 +616,7 @@ constexpr int decode_ring_stages() {
   return NW == kDecodeWideWarps ? 3 : (KV == KV_E4M3 ? 3 : 2);
 }
 
-template <bool GATHER, int D, int KV, bool QBF16, int NT, int NW>
+template <bool GATHER, int D, int KV, bool QBF16, int NT, int NW, bool FF>
 static pkv_status launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK,
                                   const CUtensorMap& tmV, cudaStream_t stream,
                                   bool programmatic) {
@@ -516,7 +625,7 @@ static pkv_status launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK,
   static_assert(NW == kDecodeWarps || (NW == kDecodeWideWarps && !GATHER),
                 "decode CTAs have kDecodeWarps warps, or kDecodeWideWarps with TMA pages");
   using Cfg = DecodeCfg<D, KV, NT, NW, NST>;
-  auto kern = decode_kernel<D, KV, QBF16, NT, NW, NST, GATHER>;
+  auto kern = decode_kernel<D, KV, QBF16, NT, NW, NST, GATHER, FF>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
   static std::atomic<bool> attr_set[64];  // per device; the call is idempotent
@@ -526,7 +635,7 @@ static pkv_status launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK,
       return PKV_ERR_CUDA;
     attr_set[dev] = true;
   }
-  dim3 grid(p.grid_parts, p.Hkv, p.B);
+  const dim3 grid = FF ? dim3(p.grid_parts * p.Hkv * p.B) : dim3(p.grid_parts, p.Hkv, p.B);
   if (programmatic) {
     // may start while the previous kernel on the stream still runs (it
     // reads nothing that kernel writes)
@@ -546,31 +655,34 @@ static pkv_status launch_decode_t(const DecodeParams& p, const CUtensorMap& tmK,
   return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-template <bool GATHER, int D, int KV, bool QBF16, int NW>
+template <bool GATHER, int D, int KV, bool QBF16, int NW, bool FF>
 static pkv_status launch_decode_nt(const DecodeParams& p, const CUtensorMap& tmK,
                                    const CUtensorMap& tmV, cudaStream_t stream, bool prog) {
   if constexpr (D <= 128) {
-    if (p.G > 8) return launch_decode_t<GATHER, D, KV, QBF16, 2, NW>(p, tmK, tmV, stream, prog);
+    if (p.G > 8)
+      return launch_decode_t<GATHER, D, KV, QBF16, 2, NW, FF>(p, tmK, tmV, stream, prog);
   } else {
     if (p.G > 8) return PKV_ERR_UNSUPPORTED;        // 16 head columns at D = 256: not built
   }
-  return launch_decode_t<GATHER, D, KV, QBF16, 1, NW>(p, tmK, tmV, stream, prog);
+  return launch_decode_t<GATHER, D, KV, QBF16, 1, NW, FF>(p, tmK, tmV, stream, prog);
 }
 
-template <bool GATHER, int D, int NW>
+template <bool GATHER, int D, int NW, bool FF>
 static pkv_status launch_decode_d(const DecodeParams& p, pkv_dtype q_dtype, pkv_dtype kv_dtype,
                                   const CUtensorMap& tmK, const CUtensorMap& tmV,
                                   cudaStream_t stream, bool prog) {
   const bool qbf = (q_dtype == PKV_BF16);
   if (kv_dtype == PKV_FP8_E4M3)
-    return qbf ? launch_decode_nt<GATHER, D, KV_E4M3, true, NW>(p, tmK, tmV, stream, prog)
-               : launch_decode_nt<GATHER, D, KV_E4M3, false, NW>(p, tmK, tmV, stream, prog);
+    return qbf ? launch_decode_nt<GATHER, D, KV_E4M3, true, NW, FF>(p, tmK, tmV, stream, prog)
+               : launch_decode_nt<GATHER, D, KV_E4M3, false, NW, FF>(p, tmK, tmV, stream, prog);
   if (kv_dtype == PKV_BF16)
-    return launch_decode_nt<GATHER, D, KV_BF16, true, NW>(p, tmK, tmV, stream, prog);
-  return launch_decode_nt<GATHER, D, KV_F16, false, NW>(p, tmK, tmV, stream, prog);
+    return launch_decode_nt<GATHER, D, KV_BF16, true, NW, FF>(p, tmK, tmV, stream, prog);
+  return launch_decode_nt<GATHER, D, KV_F16, false, NW, FF>(p, tmK, tmV, stream, prog);
 }
 
-template <bool GATHER, int NW = kDecodeWarps>
+// GATHER: pages gathered row by row (blocks below 16 tokens); NW: warps per
+// CTA; FF: full-first CTA order (decode_item_full_first).
+template <bool GATHER, int NW = kDecodeWarps, bool FF = false>
 pkv_status launch_decode_mode(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                               pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
                               cudaStream_t stream, bool prog) {
@@ -579,10 +691,10 @@ pkv_status launch_decode_mode(const DecodeParams& p, int head_dim, pkv_dtype q_d
     if (head_dim == 256) return PKV_ERR_UNSUPPORTED;
   } else {
     if (head_dim == 256)
-      return launch_decode_d<GATHER, 256, NW>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);
+      return launch_decode_d<GATHER, 256, NW, FF>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);
   }
   if (head_dim == 128)
-    return launch_decode_d<GATHER, 128, NW>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);
-  return launch_decode_d<GATHER, 64, NW>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);
+    return launch_decode_d<GATHER, 128, NW, FF>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);
+  return launch_decode_d<GATHER, 64, NW, FF>(p, q_dtype, kv_dtype, tmK, tmV, stream, prog);
 }
 }  // namespace pkv

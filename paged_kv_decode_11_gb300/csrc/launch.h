@@ -16,6 +16,7 @@ constexpr int kGatherMaxPartitionTokens = 2048;   // split-KV partition cap (blo
 constexpr int kDecodeWorkers = 4;           // resident decode CTAs per SM assumed by the planner
 constexpr int kDecodeWarps = 4;             // warps per decode CTA
 constexpr int kDecodeWideWarps = 8;         // warps per whole-context decode CTA
+constexpr int kFullFirstMaxSeqs = 256;      // batches the full-first CTA order takes
 
 struct DecodeParams {
   void* out;
@@ -40,6 +41,7 @@ struct DecodeParams {
                               // take the CTA partition's pages round-robin
   int grid_parts;             // CTAs per (sequence, KV head) in the grid
   int wide;                   // (host routing) whole-context CTAs of kDecodeWideWarps warps
+  int full_first;             // 1-D grid in full-first (longest-first) order of work items
   float qk_scale_log2;        // scale * log2(e)
   int wait_prior;             // wait for the grids ahead of it on the stream before reading
   // early start (per-partition kernel, TMA pages): the kernel ahead of it is
@@ -106,6 +108,11 @@ pkv_status launch_decode(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
 pkv_status launch_decode_wide(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                               pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
                               cudaStream_t stream, bool programmatic);
+// Decode in full-first CTA order (p.full_first), pages loaded by TMA.
+pkv_status launch_decode_full_first(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
+                                    pkv_dtype kv_dtype, const CUtensorMap& tmK,
+                                    const CUtensorMap& tmV, cudaStream_t stream,
+                                    bool programmatic);
 // Decode for blocks of fewer than 16 tokens (pages gathered row by row).
 pkv_status launch_decode_gather(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                                 pkv_dtype kv_dtype, cudaStream_t stream, bool programmatic);
