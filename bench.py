@@ -178,8 +178,8 @@ class ClockSampler:
 
 # The device code the decode kernels are built from and their partition
 # planner: a traffic figure ncu took stays valid while none of these changes.
-DECODE_SOURCES = ("common.cuh", "decode.cu", "decode_frags.cuh",
-                  "decode_kernel.cuh", "launch.h", "plan.h", "ptx.cuh")
+DECODE_SOURCES = ("common.cuh", "decode.cu", "decode_frags.cuh", "decode_full_first.cu",
+                  "decode_kernel.cuh", "decode_wide.cu", "launch.h", "plan.h", "ptx.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_traffic.json")
 
 

@@ -262,14 +262,8 @@ pkv_status decode_setup(void* out, const void* q, pkv_dtype q_dtype, const void*
                        bs_log2, head_dim, plan_ctas_per_sm) ? 1 : 0;
   if (p.wide) p.part = std::max(16, (max_seq_len + 15) / 16 * 16);   // one partition
   p.grid_parts = std::max(1, (max_seq_len + p.part - 1) / p.part);
-  // Longest-first CTA order, for decode planned beside a prefill grid (one
-  // resident CTA per SM) when contexts are split and the batch is small
-  // enough for every CTA to rank its sequences. Measured on its own, decode
-  // loses with it (the equal full partitions it puts first start and end in
-  // step, so whole waves drain at once); beside the prefill it wins.
-  p.full_first = (plan_ctas_per_sm == 1 && !p.wide && p.grid_parts > 1 && bs_log2 >= 4 &&
-                  num_seqs <= kFullFirstMaxSeqs &&
-                  (int64_t)p.grid_parts * num_kv_heads * num_seqs < (int64_t)1 << 31) ? 1 : 0;
+  p.full_first = full_first_order(num_seqs, num_kv_heads, p.grid_parts, bs_log2,
+                                  plan_ctas_per_sm, p.wide != 0) ? 1 : 0;
   p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   p.wait_prior = 1;
   return PKV_OK;

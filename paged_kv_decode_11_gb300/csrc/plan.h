@@ -68,6 +68,19 @@ inline bool wide_decode(int64_t units, int sms, int max_seq_len, int partition_t
   return max_seq_len <= 4096 && units * 4 >= (int64_t)sms * 3;
 }
 
+// Longest-first CTA order (decode_item_full_first in decode_kernel.cuh), for
+// decode planned beside a prefill grid (one resident CTA per SM) when
+// contexts are split, pages are loaded by TMA and the batch is small enough
+// for every CTA to rank its sequences. Measured on its own, decode loses with
+// it (the equal full partitions it puts first start and end in step, so
+// whole waves drain at once); beside the prefill it wins.
+inline bool full_first_order(int num_seqs, int num_kv_heads, int grid_parts, int bs_log2,
+                             int ctas_per_sm, bool wide) {
+  return ctas_per_sm == 1 && !wide && grid_parts > 1 && bs_log2 >= 4 &&
+         num_seqs <= kFullFirstMaxSeqs &&
+         (int64_t)grid_parts * num_kv_heads * num_seqs < ((int64_t)1 << 31);
+}
+
 // Tokens of the partition each warp of a decode CTA reduces on its own, or 0.
 // With an explicit partition size (blocks of 16 tokens or more, pages loaded
 // by TMA) the kDecodeWarps warps of a CTA take consecutive partitions of one
