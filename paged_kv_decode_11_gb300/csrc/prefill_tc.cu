@@ -60,16 +60,25 @@ constexpr float kRescaleLog2 = 8.f;           // reference-max slack (log2 units
 // own, not the prefill half of a varlen step).
 template <int D, int NST, bool KV8 = false, bool ALONE = true>
 struct PrefillTcCfg {
-  static constexpr int NG = D <= 128 ? 2 : 1;
+  // 128-key tiles (WIDE): one softmax group over two S buffers in tensor
+  // memory, P written over its own S; otherwise two groups up to D = 128
+  static constexpr bool WIDE = ALONE && !KV8 && D <= 128;
+  static constexpr int NG = WIDE ? 1 : (D <= 128 ? 2 : 1);
   // keys per tile (the S MMA's N): 128 for 16-bit caches at D <= 128 running
   // alone, with one S buffer (TMEM) and one P buffer (shared) per group; 64
   // otherwise, with two. Beside a decode grid the 64-key kernel, whose loads
   // press less on L2, made the varlen step faster (102.7 against 104.4 us on
   // the mixed step), while alone the 128-key one is faster at every size.
-  static constexpr bool WIDE = ALONE && !KV8 && D <= 128;
   static constexpr int KEYS = WIDE ? 128 : 64;
   static constexpr int PAGES = KEYS / kBS;                   // 16-token pages per tile
-  static constexpr int NSB = WIDE ? 1 : 2;                   // S and P buffers per group
+  // S (and P) buffers per group: three for the one group of 128-key tiles
+  // (3 x 128 S columns and 128 of O fill the 512), so an S product waits for
+  // the P.V two tiles back, not the one before
+  static constexpr int NSB = WIDE ? 3 : 2;
+  // P in tensor memory (128-key tiles): the softmax writes P over its own S
+  // columns (two 16-bit values per 32-bit column) and the P.V MMAs read it
+  // there, which frees the shared P buffers for deeper K and V rings
+  static constexpr bool PTM = WIDE;
   static constexpr int PK = WIDE ? 4 : 1;
   static constexpr int PV = WIDE ? 3 : 1;
   static constexpr int WARPS = 4 * NG + PK + 1 + PV;
@@ -97,7 +106,7 @@ struct PrefillTcCfg {
   static constexpr int STG_PAGE = kBS * D;                   // one E4M3 page
   static constexpr int STG_BYTES = PAGES * STG_PAGE;         // one staged E4M3 tile
   static constexpr int SMEM_BYTES =
-      1024 + Q_BYTES + 2 * RING_BYTES + NSB * NG * P_BYTES + 2 * NSS * STG_BYTES;
+      1024 + Q_BYTES + 2 * RING_BYTES + (PTM ? 0 : NSB * NG * P_BYTES) + 2 * NSS * STG_BYTES;
   static constexpr uint32_t TMEM_COLS = 512;                  // 2 S buffers and O per group
   static_assert(NG * (NSB * KEYS + D) <= (int)TMEM_COLS, "tensor memory");
 };
@@ -196,10 +205,11 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
   __shared__ uint64_t full_k[NST], empty_k[NST], full_v[NST], empty_v[NST];
   __shared__ uint64_t stg_k[NSS], stg_v[NSS];           // KV8: staged E4M3 tile landed
   // per softmax group g and buffer b: S ready, P written, P.V done
-  __shared__ uint64_t s_bar[NG][2], o_bar[NG][2], p_bar[NG][2];
+  __shared__ uint64_t s_bar[NG][NSB], o_bar[NG][NSB], p_bar[NG][NSB];
   __shared__ uint64_t ready_bar, recv_bar;              // cluster hand-off (SPLIT == 2)
+  __shared__ uint64_t done_bar;                         // PTM: every MMA of the CTA is done
   __shared__ uint32_t tmem_base;
-  __shared__ float s_qpow[kTcRows];                     // KV8, bf16 q: 2^shift of each row
+  __shared__ float s_qpow[KV8 ? kTcRows : 1];           // KV8, bf16 q: 2^shift of each row
 
   // a decode launched behind this kernel as a programmatic dependent may take
   // the SM room this grid leaves as soon as all of its CTAs are running
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
   uint8_t* pKV = basep + Cfg::Q_BYTES;
   uint8_t* pV = pKV + Cfg::RING_BYTES;
   uint8_t* pP = pV + Cfg::RING_BYTES;
-  uint8_t* pStg = pP + NSB * NG * Cfg::P_BYTES;        // KV8: K staging, then V staging
+  uint8_t* pStg = pP + (Cfg::PTM ? 0 : NSB * NG * Cfg::P_BYTES);   // KV8: K, then V staging
 
   bool failed = false;                                  // a wait ran out: stop waiting
   auto wait = [&](uint64_t* bar, uint32_t parity) {
@@ -371,13 +381,14 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
         mbar_init(&stg_v[s], 1);
       }
       for (int g = 0; g < NG; ++g)
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NSB; ++b) {
           mbar_init(&s_bar[g][b], 1);
           mbar_init(&o_bar[g][b], 1);
           mbar_init(&p_bar[g][b], kTcRows);             // every thread of the group
         }
       mbar_init(&ready_bar, 1);
       mbar_init(&recv_bar, NG * kTcRows);
+      mbar_init(&done_bar, 1);
       fence_barrier_init();
     }
     __syncwarp();
@@ -482,45 +493,69 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
       if (lane == 0) {
         int us = 0, up = 0;                               // next S, next P.V
         uint32_t idle = 0;
-        while (up < n_tiles && !failed) {
-          if (us < n_tiles && us < up + NSB * NG &&
-              mbar_test_wait(&full_k[us % NST], (us / NST) & 1)) {
-            const int g = us % NG, j = us / NG;
-            tc::fence_after();
-            const uint32_t kst = sKV + (us % NST) * Cfg::KV_BYTES;
+        // PTM: the P.V that read P from this S buffer (its previous tile)
+        // must be complete, not just issued, before S overwrites it
+        auto s_ready = [&]() {
+          return us < n_tiles && us < up + NSB * NG &&
+                 mbar_test_wait(&full_k[us % NST], (us / NST) & 1) &&
+                 (!Cfg::PTM || us < NSB * NG ||
+                  mbar_test_wait(&o_bar[us % NG][(us / NG) % NSB], (((us / NG) - NSB) / NSB) & 1));
+        };
+        auto s_issue = [&]() {
+          const int g = us % NG, j = us / NG;
+          tc::fence_after();
+          const uint32_t kst = sKV + (us % NST) * Cfg::KV_BYTES;
   #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-              const uint32_t ko = (k % 4) * 32u;
-              const uint64_t a = tc::sdesc(sQ + (k / 4) * Cfg::Q_BOX + ko, 16, 1024);
-              const uint64_t bd = tc::sdesc(kst + (k / 4) * Cfg::KV_BOX + ko, 16, 1024);
-              tc::mma(tS + (NSB * g + j % NSB) * kTcKeys, a, bd, ID_S, k > 0 ? 1u : 0u);
-            }
-            tc::commit(&s_bar[g][j % NSB]);
-            tc::commit(&empty_k[us % NST]);               // the K stage is free once S is done
-            ++us;
-            idle = 0;
-          } else if (up < us &&
-                     mbar_test_wait(&p_bar[up % NG][(up / NG) % NSB], ((up / NG) / NSB) & 1) &&
-                     mbar_test_wait(&full_v[up % NST], (up / NST) & 1)) {
-            const int g = up % NG, j = up / NG, b = j % NSB;
-            tc::fence_after();
-            const uint32_t vst = sV + (up % NST) * Cfg::KV_BYTES;
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t ko = (k % 4) * 32u;
+            const uint64_t a = tc::sdesc(sQ + (k / 4) * Cfg::Q_BOX + ko, 16, 1024);
+            const uint64_t bd = tc::sdesc(kst + (k / 4) * Cfg::KV_BOX + ko, 16, 1024);
+            tc::mma(tS + (NSB * g + j % NSB) * kTcKeys, a, bd, ID_S, k > 0 ? 1u : 0u);
+          }
+          tc::commit(&s_bar[g][j % NSB]);
+          tc::commit(&empty_k[us % NST]);                 // the K stage is free once S is done
+          ++us;
+        };
+        auto pv_ready = [&]() {
+          return up < us && mbar_test_wait(&p_bar[up % NG][(up / NG) % NSB], ((up / NG) / NSB) & 1) &&
+                 mbar_test_wait(&full_v[up % NST], (up / NST) & 1);
+        };
+        auto pv_issue = [&]() {
+          const int g = up % NG, j = up / NG, b = j % NSB;
+          tc::fence_after();
+          const uint32_t vst = sV + (up % NST) * Cfg::KV_BYTES;
   #pragma unroll
-            for (int k = 0; k < kTcKeys / 16; ++k) {
+          for (int k = 0; k < kTcKeys / 16; ++k) {
+            const uint64_t bd = tc::sdesc(vst + k * 2 * 1024, Cfg::KV_BOX, 1024);
+            if constexpr (Cfg::PTM) {
+              // 16 keys of P: 8 columns of the group's S buffer
+              tc::mma_ts(tO + g * D, tS + (NSB * g + b) * kTcKeys + 8 * k, bd, ID_O,
+                         (j > 0 || k > 0) ? 1u : 0u);
+            } else {
               const uint64_t a = tc::sdesc(
-                  sP + (NSB * g + b) * Cfg::P_BYTES + (k / 4) * Cfg::P_CB + (k % 4) * 32, 16, 1024);
-              const uint64_t bd = tc::sdesc(vst + k * 2 * 1024, Cfg::KV_BOX, 1024);
+                  sP + (NSB * g + b) * Cfg::P_BYTES + (k / 4) * Cfg::P_CB + (k % 4) * 32, 16,
+                  1024);
               tc::mma(tO + g * D, a, bd, ID_O, (j > 0 || k > 0) ? 1u : 0u);
             }
-            tc::commit(&o_bar[g][b]);
-            tc::commit(&empty_v[up % NST]);               // the V stage is free once P.V is done
-            ++up;
+          }
+          tc::commit(&o_bar[g][b]);
+          tc::commit(&empty_v[up % NST]);                 // the V stage is free once P.V is done
+          ++up;
+        };
+        while (up < n_tiles && !failed) {
+          // S products first: the softmax waits on them
+          bool did = true;
+          if (s_ready()) s_issue();
+          else if (pv_ready()) pv_issue();
+          else did = false;
+          if (did) {
             idle = 0;
           } else if (++idle > (1u << 26)) {
             failed = true;                                // nothing became ready: give up
             atomicOr(p.err, PKV_DEVERR_TIMEOUT);
           }
         }
+        if constexpr (Cfg::PTM) tc::commit(&done_bar);  // once every MMA above is complete
       }
       __syncwarp();
       if constexpr (SPLIT > 1) cluster_wait();
@@ -610,6 +645,9 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
 #pragma unroll
     for (int hh = 0; hh < HALVES; ++hh) {
       if (HALVES > 1) load_half(hh);                    // (one half: x still holds it)
+      // PTM: P of keys 64 hh .. 64 hh + 63 goes to columns 32 hh .. 32 hh + 31
+      // of the S buffer, which hold scores of keys already read into x
+      uint32_t pv[32];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         float e[8];
@@ -620,9 +658,18 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
         }
         const uint4 w = make_uint4(pack16x2<BF16>(e[0], e[1]), pack16x2<BF16>(e[2], e[3]),
                                    pack16x2<BF16>(e[4], e[5]), pack16x2<BF16>(e[6], e[7]));
-        *reinterpret_cast<uint4*>(pPb + hh * Cfg::P_CB + swz128(r, c)) = w;
+        if constexpr (Cfg::PTM) {
+          pv[4 * c] = w.x;
+          pv[4 * c + 1] = w.y;
+          pv[4 * c + 2] = w.z;
+          pv[4 * c + 3] = w.w;
+        } else {
+          *reinterpret_cast<uint4*>(pPb + hh * Cfg::P_CB + swz128(r, c)) = w;
+        }
       }
+      if constexpr (Cfg::PTM) tc::st32(sbuf + hh * 32, pv);
     }
+    if constexpr (Cfg::PTM) tc::wait_st();
 #pragma unroll
     for (int w = 4; w > 0; w >>= 1)
 #pragma unroll
@@ -659,11 +706,19 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
   // Combined: M = max(m_0, m_1), O = O_0 w_0 + O_1 w_1 with w_g = 2^(m_g - M),
   // and the same for the sum. (reference max, sum) of each row go through the
   // group's first P buffer, which its last P.V has finished reading.
-  reinterpret_cast<float2*>(pP + NSB * grp * Cfg::P_BYTES)[r] = make_float2(m_ref, l);
+  // (PTM: through the query tile's space, once every MMA, the S products
+  // that read it included, is complete)
+  if constexpr (Cfg::PTM) {
+    wait(&done_bar, 0);
+    tc::fence_after();
+  }
+  float2* ml_g0 = Cfg::PTM ? reinterpret_cast<float2*>(pQ) : reinterpret_cast<float2*>(pP);
+  float2* ml_g1 = Cfg::PTM ? reinterpret_cast<float2*>(pQ) + kTcRows
+                           : reinterpret_cast<float2*>(pP + NSB * Cfg::P_BYTES);
+  (grp == 0 ? ml_g0 : ml_g1)[r] = make_float2(m_ref, l);
   named_barrier(1, NG * kTcRows);
-  const float2 ml0 = reinterpret_cast<const float2*>(pP)[r];
-  const float2 ml1 = NG > 1 ? reinterpret_cast<const float2*>(pP + NSB * Cfg::P_BYTES)[r]
-                            : make_float2(-INFINITY, 0.f);
+  const float2 ml0 = ml_g0[r];
+  const float2 ml1 = NG > 1 ? ml_g1[r] : make_float2(-INFINITY, 0.f);
   // a group with no tile has no O
   const bool has0 = n_tiles > 0, has1 = NG > 1 && n_tiles > 1;
   const float M = fmaxf(ml0.x, ml1.x);
@@ -763,8 +818,10 @@ template <int D, int KV, bool QBF16, int SPLIT, bool ALONE>
 static pkv_status launch_prefill_tc_s(const PrefillParams& q, const CUtensorMap& tmK,
                                       const CUtensorMap& tmV, cudaStream_t stream, int dev) {
   constexpr bool KV8 = KV == KV_E4M3;
-  // ring stages: 2 for the 128-key tiles at D = 128 (32 KB each), for E4M3 and D = 256
-  constexpr int NST = (D > 128 || KV8 || (ALONE && D == 128)) ? 2 : 4;
+  // ring stages: the 128-key tiles (P in tensor memory) take 3 of 32 KB at
+  // D = 128 and 6 of 16 KB at D = 64; E4M3 and D = 256 take 2, the rest 4
+  constexpr bool WIDE = PrefillTcCfg<D, 2, KV8, ALONE>::WIDE;
+  constexpr int NST = WIDE ? (D == 128 ? 3 : 6) : ((D > 128 || KV8) ? 2 : 4);
   using Cfg = PrefillTcCfg<D, NST, KV8, ALONE>;
   static_assert(Cfg::SMEM_BYTES + 512 <= 227 * 1024, "shared memory (dynamic + static)");
   static_assert(SPLIT == 1 || kTcRows * (D / SPLIT) * 4 + kTcRows * 8 <= 2 * Cfg::RING_BYTES,

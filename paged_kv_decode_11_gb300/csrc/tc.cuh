@@ -73,6 +73,18 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] . B[smem]: the same MMA with A read from tensor memory
+// (row i of A in lane i, two 16-bit elements per 32-bit column, K-major; a
+// 16-element K step spans 8 columns).
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
 // One arrival on `bar` once every MMA this thread issued so far is complete.
 __device__ __forceinline__ void commit(uint64_t* bar) {
   asm volatile(
