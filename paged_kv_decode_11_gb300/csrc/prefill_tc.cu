@@ -528,9 +528,10 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
           for (int k = 0; k < kTcKeys / 16; ++k) {
             const uint64_t bd = tc::sdesc(vst + k * 2 * 1024, Cfg::KV_BOX, 1024);
             if constexpr (Cfg::PTM) {
-              // 16 keys of P: 8 columns of the group's S buffer
-              tc::mma_ts(tO + g * D, tS + (NSB * g + b) * kTcKeys + 8 * k, bd, ID_O,
-                         (j > 0 || k > 0) ? 1u : 0u);
+              // 16 keys of P: 8 columns of the group's S buffer, each
+              // 64-key half of P at the start of that half's S columns
+              tc::mma_ts(tO + g * D, tS + (NSB * g + b) * kTcKeys + 64 * (k / 4) + 8 * (k % 4),
+                         bd, ID_O, (j > 0 || k > 0) ? 1u : 0u);
             } else {
               const uint64_t a = tc::sdesc(
                   sP + (NSB * g + b) * Cfg::P_BYTES + (k / 4) * Cfg::P_CB + (k % 4) * 32, 16,
@@ -643,10 +644,13 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
 #pragma unroll
     for (int k = 0; k < 8; ++k) rs8[k] = 0.f;
 #pragma unroll
-    for (int hh = 0; hh < HALVES; ++hh) {
-      if (HALVES > 1) load_half(hh);                    // (one half: x still holds it)
-      // PTM: P of keys 64 hh .. 64 hh + 63 goes to columns 32 hh .. 32 hh + 31
-      // of the S buffer, which hold scores of keys already read into x
+    for (int it = 0; it < HALVES; ++it) {
+      // PTM: the last half first, from the registers the max pass left it in,
+      // then the others reloaded; P of keys 64 hh .. 64 hh + 63 goes to
+      // columns 64 hh .. 64 hh + 31, the first half of that half's own scores
+      // (already in x), so no score is overwritten before it is read
+      const int hh = Cfg::PTM ? HALVES - 1 - it : it;
+      if (HALVES > 1 && (!Cfg::PTM || it > 0)) load_half(hh);   // (else x holds it)
       uint32_t pv[32];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
@@ -667,7 +671,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
           *reinterpret_cast<uint4*>(pPb + hh * Cfg::P_CB + swz128(r, c)) = w;
         }
       }
-      if constexpr (Cfg::PTM) tc::st32(sbuf + hh * 32, pv);
+      if constexpr (Cfg::PTM) tc::st32(sbuf + hh * 64, pv);
     }
     if constexpr (Cfg::PTM) tc::wait_st();
 #pragma unroll
@@ -690,7 +694,9 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
             make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    fence_proxy_async_smem();                           // P and the zeros, for the tensor cores
+    // P (shared memory) and the zeros, for the tensor cores; with P in tensor
+    // memory only the zeros need it
+    if (!Cfg::PTM || (!KV8 && vz < kTcKeys)) fence_proxy_async_smem();
     tc::fence_before();
     mbar_arrive(&p_bar[grp][b]);
   }
