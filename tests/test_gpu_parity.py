@@ -145,6 +145,18 @@ def test_decode_automatic_plan_either_side_of_one_cta_per_sm(extra, kv):
     _decode_vs_oracle(c, partition_tokens=0)
 
 
+@pytest.mark.parametrize("kv", ["same", "fp8"])
+def test_decode_merge_in_several_chunks(kv):
+    # G = 16 at D = 128: one partition's partial is 16 rows of 128 fp32, so the
+    # merging CTA's shared memory holds a few partitions at a time and a head's
+    # 16 CTA partials (16-token partitions, 4 per CTA, 1000-token contexts)
+    # arrive in several bulk-copy rounds
+    ctx = [1000, 999, 1, 64, 65, 700]
+    c = make_case("tiny", 6, B=len(ctx), Hq=32, Hkv=2, D=128, dtype="bf16", kv=kv,
+                  ctx=("fixed", ctx), pool=("scale", 1.5))
+    _decode_vs_oracle(c, partition_tokens=16)
+
+
 def test_decode_empty_sequences():
     c = make_case("tiny", 5, ctx=("fixed", [0, 40, 0, 1]))
     kc, vc = product_cache(c)
