@@ -562,10 +562,11 @@ __global__ void __launch_bounds__(NW * 32)
       const int hh = i / n, sp = i - hh * n;
       s_lse[hh * CH + sp] = ldcg_f32(lse_rows + hh * p.max_parts + c0 + sp);
     }
-    __syncthreads();
-    if (!mbar_wait_bounded(&s_mbar, ci & 1)) {
-      // leave only once the copies have landed (bounded): they target this
-      // CTA's shared memory
+    // the vote is also the barrier that publishes the log2-sum-exps; a CTA
+    // whose copies did not all land leaves as one, after waiting once more
+    // (bounded), since they target its own shared memory
+    const bool landed = mbar_wait_bounded(&s_mbar, ci & 1);
+    if (__syncthreads_or(!landed)) {
       if (tid == 0) atomicOr(p.err, PKV_DEVERR_TIMEOUT);
       mbar_wait_bounded(&s_mbar, ci & 1);
       return;
