@@ -115,6 +115,7 @@ SHAPES = [
     (64, 8, 2, "f16", "same"), (128, 8, 8, "bf16", "same"), (128, 28, 4, "bf16", "same"),
     (128, 32, 8, "bf16", "fp8"), (128, 16, 1, "f16", "fp8"), (64, 16, 2, "bf16", "fp8"),
     (128, 32, 2, "f16", "same"), (64, 12, 12, "bf16", "same"), (128, 14, 2, "bf16", "fp8"),
+    (64, 32, 2, "bf16", "fp8"),
 ]
 
 

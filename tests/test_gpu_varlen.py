@@ -64,10 +64,10 @@ def test_mixed_step_varlen_vs_oracle_and_two_streams(kv, part):
     assert_close(one.prefill_lse, plse, LSE_TOL, "varlen chunk lse")
 
 
-def _batch(seed, n_dec, chunks, kv="same", BS=16):
+def _batch(seed, n_dec, chunks, kv="same", BS=16, ctx_dec=None):
     """A batch of n_dec decode sequences and one chunk sequence per (L, P)."""
     rng = np.random.default_rng(seed)
-    ctx_dec = list(rng.integers(1, 900, n_dec))
+    ctx_dec = list(rng.integers(1, 900, n_dec)) if ctx_dec is None else list(ctx_dec)
     c = make_case("tiny", seed, B=n_dec + len(chunks), BS=BS, Hq=16, Hkv=4, D=128,
                   dtype="bf16", kv=kv, ctx=("fixed", ctx_dec + [L + Pp for L, Pp in chunks]),
                   pool=("scale", 1.3))
@@ -98,6 +98,28 @@ def test_varlen_batch_vs_oracle(n_dec, chunks, kv):
     check_device_ok()
     ko, vo = oracle_cache(c)
     # every row of the batch is causal attention of its token over its own context
+    want, wlse = O.prefill_chunk(q, ko, vo, c.block_tables, c.seq_lens, qsl, c.scale,
+                                 c.k_scales, c.v_scales)
+    assert_close(out, want, tol(c), "varlen rows")
+    assert_close(lse, wlse, LSE_TOL, "varlen lse")
+
+
+@pytest.mark.parametrize("kv", ["same", "fp8"])
+def test_varlen_decode_contexts_on_partition_boundaries(kv):
+    # beside a chunk the decode CTAs take their work in full-first order:
+    # every full partition, then the shorter last ones by decreasing length;
+    # contexts that end exactly on a partition boundary have no short one
+    ctx_dec = [512, 1024, 1, 513, 1535, 1536, 2048, 700, 16, 17]
+    c, q, qsl = _batch(41, len(ctx_dec), [(64, 200)], kv, ctx_dec=ctx_dec)
+    kc, vc = product_cache(c)
+    ks, vs = scales(c)
+    out = torch.empty_like(q).cuda()
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    P.paged_attn_varlen(out, dev(q), kc, vc, dev(c.block_tables), dev(c.seq_lens), dev(qsl),
+                        len(ctx_dec), float(c.scale), 64, int(max(ctx_dec)), ks, vs, out_lse=lse)
+    torch.cuda.synchronize()
+    check_device_ok()
+    ko, vo = oracle_cache(c)
     want, wlse = O.prefill_chunk(q, ko, vo, c.block_tables, c.seq_lens, qsl, c.scale,
                                  c.k_scales, c.v_scales)
     assert_close(out, want, tol(c), "varlen rows")
