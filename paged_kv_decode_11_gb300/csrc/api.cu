@@ -14,6 +14,8 @@
 #include "../../include/pkv.h"
 #pragma GCC visibility pop
 #include "launch.h"
+#include "launch_prefill.h"
+#include "launch_cache.h"
 #include "plan.h"
 #include "ptx.cuh"
 
@@ -117,6 +119,24 @@ bool make_kv_tmap(CUtensorMap* m, const void* base, pkv_dtype dt, int D, int Hkv
   CUresult r = fn(m, t, 3, const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE,
                   box_row == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Tensor map {D, Hq, rows} over the 16-bit queries [rows, Hq, D] of a
+// prefill: one box is 64 elements (128 bytes, swizzled like the K and V boxes)
+// of the G heads of one KV head over q_tile consecutive tokens, which are the
+// (token, head) rows of a tensor-core query tile in the tile's row order.
+// Tokens past the last row read as zeros.
+bool make_q_tmap(CUtensorMap* m, const void* q, int D, int Hq, int G, int q_tile, int rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hq * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)q_tile};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(q), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -289,7 +309,7 @@ pkv_status decode_launch(const DecodeCall& c, cudaStream_t stream, bool beside_p
 
 struct PrefillCall {
   PrefillParams p;
-  CUtensorMap tmK, tmV;
+  CUtensorMap tmQ, tmK, tmV;
   int head_dim;
   pkv_dtype q_dtype, kv_dtype;
   bool empty;
@@ -301,7 +321,7 @@ pkv_status prefill_setup(void* out, const void* q, pkv_dtype q_dtype, const void
                          int total_q_tokens, int max_q_len, int num_q_heads, int num_kv_heads,
                          int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
                          float scale, const float* k_scales, const float* v_scales,
-                         float* out_lse, PrefillCall* call) {
+                         float* out_lse, int q_rows, PrefillCall* call) {
   call->empty = true;
   if (num_seqs < 0 || total_q_tokens < 0 || max_q_len < 0 || num_q_heads <= 0 ||
       num_kv_heads <= 0 || max_blocks_per_seq <= 0 || num_blocks <= 0)
@@ -326,6 +346,10 @@ pkv_status prefill_setup(void* out, const void* q, pkv_dtype q_dtype, const void
     return PKV_ERR_INVALID_ARG;
   if (!make_kv_tmap(&call->tmK, k_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift) ||
       !make_kv_tmap(&call->tmV, v_cache, kv_dtype, head_dim, num_kv_heads, num_blocks, shift))
+    return PKV_ERR_CUDA;
+  call->tmQ = CUtensorMap{};
+  if (kv_dtype != PKV_FP8_E4M3 && prefill_tc_supported(head_dim, kv_dtype) &&
+      !make_q_tmap(&call->tmQ, q, head_dim, num_q_heads, G, kPrefillTcRows / G, q_rows))
     return PKV_ERR_CUDA;
   unsigned int* err = err_word();
   if (err == nullptr) return PKV_ERR_CUDA;
@@ -361,7 +385,7 @@ pkv_status prefill_setup(void* out, const void* q, pkv_dtype q_dtype, const void
 pkv_status prefill_launch(const PrefillCall& c, cudaStream_t stream, bool beside_decode) {
   if (c.empty) return PKV_OK;
   if (prefill_tc_supported(c.head_dim, c.kv_dtype))
-    return launch_prefill_tc(c.p, c.head_dim, c.q_dtype, c.kv_dtype, c.tmK, c.tmV, stream,
+    return launch_prefill_tc(c.p, c.head_dim, c.q_dtype, c.kv_dtype, c.tmQ, c.tmK, c.tmV, stream,
                              !beside_decode);
   return launch_prefill(c.p, c.head_dim, c.q_dtype, c.kv_dtype, c.tmK, c.tmV, stream);
 }
@@ -429,7 +453,7 @@ pkv_status paged_attn_prefill_chunk(void* out, const void* q, pkv_dtype q_dtype,
                                 seq_lens, cu_q_lens, num_seqs, total_q_tokens, max_q_len,
                                 num_q_heads, num_kv_heads, head_dim, block_size,
                                 max_blocks_per_seq, num_blocks, scale, k_scales, v_scales,
-                                out_lse, &c);
+                                out_lse, total_q_tokens, &c);
   if (st != PKV_OK || c.empty) return st;
   return prefill_launch(c, reinterpret_cast<cudaStream_t>(stream), false);
 }
@@ -472,7 +496,7 @@ pkv_status paged_attn_varlen(void* out, const void* q, pkv_dtype q_dtype, const 
                      query_start_loc ? query_start_loc + num_decode_seqs : nullptr, n_pf,
                      total_q_tokens - num_decode_seqs, max_q_len, num_q_heads, num_kv_heads,
                      head_dim, block_size, max_blocks_per_seq, num_blocks, scale, k_scales,
-                     v_scales, out_lse, &pc);
+                     v_scales, out_lse, total_q_tokens, &pc);
   if (st != PKV_OK) return st;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // the prefill chunks, then decode launched as a programmatic dependent of

@@ -1,5 +1,7 @@
-// launch.h — host-side parameter blocks and launchers shared by the
-// translation units of libpkv (not part of the public ABI).
+// launch.h — host-side parameter block and launchers of decode attention,
+// and the constants its planner shares with the entry points (not part of
+// the public ABI). launch_prefill.h and launch_cache.h hold those of the
+// prefill and of the cache writes.
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -51,51 +53,6 @@ struct DecodeParams {
   int early;
 };
 
-struct PrefillParams {
-  void* out;
-  const void* q;
-  const int32_t* block_tables;
-  const int32_t* seq_lens;
-  const int32_t* cu_q_lens;
-  const float* k_scales;
-  const float* v_scales;
-  float* out_lse;
-  unsigned int* err;
-  int num_seqs, Hq, Hkv, G, max_blocks, num_blocks, max_q_len, q_tile;
-  int ppb_shift;              // log2(block_size / 16)
-  float qk_scale_log2;
-};
-
-struct CacheWriteParams {
-  const void* key;
-  const void* value;
-  void* k_cache;
-  void* v_cache;
-  const int64_t* slots;
-  const float* k_scales;
-  const float* v_scales;
-  unsigned int* err;
-  int num_tokens, Hkv, D, num_blocks;
-  int bs_log2;                // log2(block_size)
-};
-
-struct RopeCacheParams {
-  void* query;
-  const void* key;
-  const void* value;
-  void* k_cache;
-  void* v_cache;
-  const int64_t* slots;
-  const int64_t* positions;
-  const float* cos_sin;
-  const float* k_scales;
-  const float* v_scales;
-  unsigned int* err;
-  int64_t max_position;
-  int rot, neox, num_tokens, Hq, Hkv, D, num_blocks;
-  int bs_log2;                // log2(block_size)
-};
-
 // Each launcher validates nothing (the entry points do) and returns
 // PKV_ERR_CUDA on a launch failure.
 // programmatic: launch as a programmatic dependent of the previous kernel on
@@ -116,25 +73,5 @@ pkv_status launch_decode_full_first(const DecodeParams& p, int head_dim, pkv_dty
 // Decode for blocks of fewer than 16 tokens (pages gathered row by row).
 pkv_status launch_decode_gather(const DecodeParams& p, int head_dim, pkv_dtype q_dtype,
                                 pkv_dtype kv_dtype, cudaStream_t stream, bool programmatic);
-pkv_status launch_prefill(const PrefillParams& p, int head_dim, pkv_dtype q_dtype,
-                          pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                          cudaStream_t stream);
-pkv_status launch_cache_write(const CacheWriteParams& p, pkv_dtype src_dtype,
-                              pkv_dtype kv_dtype, cudaStream_t stream);
-pkv_status launch_rope_cache(const RopeCacheParams& p, pkv_dtype src_dtype, pkv_dtype kv_dtype,
-                             cudaStream_t stream);
-
-// Causal chunked prefill on the fifth-generation tensor cores (16-bit caches
-// at head_dim 64, 128 or 256; E4M3 caches at 64 or 128); the other cases take
-// launch_prefill. may_split: the grid may pair two CTAs per query tile (a
-// cluster splitting its keys) when one CTA per tile would leave more than
-// half of the SMs idle.
-bool prefill_tc_supported(int head_dim, pkv_dtype kv_dtype);
-pkv_status launch_prefill_tc(const PrefillParams& p, int head_dim, pkv_dtype q_dtype,
-                             pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                             cudaStream_t stream, bool may_split);
-
-// Rows of q handled by one prefill CTA for a GQA group size G.
-int prefill_q_tile(int G);
 
 }  // namespace pkv

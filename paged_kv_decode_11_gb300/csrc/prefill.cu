@@ -15,7 +15,7 @@
 // softmax over 16*KT-key tiles with m16n8k16 tensor-core products.
 #include <cuda.h>
 #include "common.cuh"
-#include "launch.h"
+#include "launch_prefill.h"
 
 namespace pkv {
 

@@ -38,12 +38,12 @@
 // back gives every operand a uniform 1 KB stride between 8-row groups.
 #include <cuda.h>
 #include "common.cuh"
-#include "launch.h"
+#include "launch_prefill.h"
 #include "tc.cuh"
 
 namespace pkv {
 
-constexpr int kTcRows = 128;                  // query rows per CTA (MMA M)
+constexpr int kTcRows = kPrefillTcRows;       // query rows per CTA (MMA M)
 constexpr float kRescaleLog2 = 8.f;           // reference-max slack (log2 units)
 
 // NG softmax groups of four warps (two up to D = 128; one at D = 256, whose O
@@ -192,7 +192,8 @@ __device__ __forceinline__ void tmem_ld(uint32_t taddr, uint32_t (&v)[N]) {
 // it). QBF16: the query and output type.
 template <int D, int KV, bool QBF16, int NST, int SPLIT, bool ALONE>
 __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::THREADS, 1)
-    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK,
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const PrefillParams p) {
   constexpr bool KV8 = KV == KV_E4M3;
   constexpr bool BF16 = KV == KV_BF16;                  // MMA operand type
@@ -208,6 +209,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
   __shared__ uint64_t s_bar[NG][NSB], o_bar[NG][NSB], p_bar[NG][NSB];
   __shared__ uint64_t ready_bar, recv_bar;              // cluster hand-off (SPLIT == 2)
   __shared__ uint64_t done_bar;                         // PTM: every MMA of the CTA is done
+  __shared__ uint64_t q_bar;                            // 16-bit cache: the query tile landed
   __shared__ uint32_t tmem_base;
   __shared__ float s_qpow[KV8 ? kTcRows : 1];           // KV8, bf16 q: 2^shift of each row
 
@@ -229,6 +231,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
   const int i0 = qt * p.q_tile;
   if (i0 >= L) return;
   const int i1 = min(L, i0 + p.q_tile);
+  const int rows_used = p.q_tile * G;                   // tile rows holding (token, head) pairs
   const int key_end = P0 + i1;                          // keys any row of the tile sees: < key_end
   const int n_pages = (key_end + kBS - 1) / kBS;
   const int n_tiles_all = (key_end + kTcKeys - 1) / kTcKeys;
@@ -365,8 +368,8 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
     if (u + NSS < n_tiles) issue(u + NSS);
   };
   if (warp == Cfg::W_K) {
-    // the K producer sets up the barriers and starts the first tiles right
-    // away, while the other warps load the query tile and allocate tensor memory
+    // the K producer sets up the barriers; the producers start the first tiles
+    // right away, while the other warps load the query tile and allocate tensor memory
     if (lane == 0) {
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
@@ -389,7 +392,15 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
       mbar_init(&ready_bar, 1);
       mbar_init(&recv_bar, NG * kTcRows);
       mbar_init(&done_bar, 1);
+      mbar_init(&q_bar, 1);
       fence_barrier_init();
+      if constexpr (!KV8) {
+        // the query tile by TMA ahead of every K and V tile: rows 0 ..
+        // rows_used - 1 of each 64-column block, tokens past the queries as zeros
+        mbar_arrive_expect_tx(&q_bar, Cfg::NBOX * rows_used * 128);
+        for (int c = 0; c < Cfg::NBOX; ++c)
+          tma_load_3d(pQ + c * Cfg::Q_BOX, &tmQ, &q_bar, c * 64, h * G, q0 + i0);
+      }
     }
     __syncwarp();
   }
@@ -397,19 +408,39 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
     z_cur = page_row(pg_begin + lane);
     z_next = page_row(pg_begin + 32 + lane);
   }
-  if (warp == Cfg::W_K)
-    for (int u = 0; u < (KV8 ? Cfg::NSS : NST) && u < n_tiles; ++u) issue(u);
+  if constexpr (KV8) {
+    if (warp == Cfg::W_K)
+      for (int u = 0; u < Cfg::NSS && u < n_tiles; ++u) issue(u);
+  } else if (producer) {
+    // the first S product needs only the query tile and K tile 0: the K
+    // producers load their shares of K tile 0 right behind the query tile, as
+    // soon as the barriers are set up (a barrier of the producer warps alone),
+    // ahead of the grid-wide burst of the other first stages, which start
+    // after the CTA barrier. (Holding that burst back until the query tile had
+    // landed made the 512-on-1500 chunk 0.6 us slower.)
+    named_barrier(2, (Cfg::PK + Cfg::PV) * 32);
+    if (k_warp && n_tiles > 0) issue(0);
+  }
   if (warp == 0) tc::alloc(&tmem_base, Cfg::TMEM_COLS);
 
-  // ---- query tile into shared memory (the last softmax group); rows past the
-  // chunk are zero ----------------------------------------------------------------
+  // ---- query tile into shared memory. 16-bit cache: by TMA (issued above), the
+  // last softmax group zeroing the rows no pair uses; rows of tokens past the
+  // chunk hold the next tokens' queries, and their keys are all masked. E4M3
+  // cache: loaded (and scaled to f16) by the last softmax group, rows past the
+  // chunk zero ----------------------------------------------------------------------
   const int grp = warp >> 2;                            // softmax group (warps 0 .. 4 NG - 1)
   const int r = tid & (kTcRows - 1);                    // this thread's tile row
-  const int rows_used = p.q_tile * G;
   const int qi = i0 + r / G;                            // query token within the chunk
   const int hq = h * G + r % G;                         // query head
   const bool rvalid = r < rows_used && qi < i1;
-  if (grp == NG - 1) {
+  if (!KV8 && grp == NG - 1 && r >= rows_used) {
+    // rows no (token, head) pair uses (G not dividing the tile): zeros
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c)
+      *reinterpret_cast<uint4*>(pQ + (c / 8) * Cfg::Q_BOX + swz128(r, c % 8)) =
+          make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (KV8 && grp == NG - 1) {
     const uint16_t* src =
         static_cast<const uint16_t*>(p.q) + ((int64_t)(q0 + (rvalid ? qi : 0)) * p.Hq +
                                              (rvalid ? hq : 0)) * D;
@@ -461,13 +492,13 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
       else tc::reg_lower<Cfg::REG_K>();
     }
     if (producer) {
-      // the other producers start once the barriers are set up (after the CTA barrier)
+      // KV8: the V producer starts once the barriers are set up (after the CTA barrier)
       if constexpr (KV8) {
         if (!k_warp)
           for (int u = 0; u < Cfg::NSS && u < n_tiles; ++u) issue(u);
         for (int u = 0; u < n_tiles; ++u) convert(u);
       } else {
-        for (int u = warp == Cfg::W_K ? NST : 0; u < n_tiles; ++u) {
+        for (int u = k_warp ? 1 : 0; u < n_tiles; ++u) {
           if (u >= NST) wait(&empty_x[u % NST], ((u / NST) - 1) & 1);
           issue(u);
         }
@@ -493,6 +524,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
       if (lane == 0) {
         int us = 0, up = 0;                               // next S, next P.V
         uint32_t idle = 0;
+        if constexpr (!KV8) wait(&q_bar, 0);             // the query tile (TMA)
         // PTM: the P.V that read P from this S buffer (its previous tile)
         // must be complete, not just issued, before S overwrites it
         auto s_ready = [&]() {
@@ -821,8 +853,9 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
 }
 
 template <int D, int KV, bool QBF16, int SPLIT, bool ALONE>
-static pkv_status launch_prefill_tc_s(const PrefillParams& q, const CUtensorMap& tmK,
-                                      const CUtensorMap& tmV, cudaStream_t stream, int dev) {
+static pkv_status launch_prefill_tc_s(const PrefillParams& q, const CUtensorMap& tmQ,
+                                      const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                      cudaStream_t stream, int dev) {
   constexpr bool KV8 = KV == KV_E4M3;
   // ring stages: the 128-key tiles (P in tensor memory) take 3 of 32 KB at
   // D = 128 and 6 of 16 KB at D = 64; E4M3 and D = 256 take 2, the rest 4
@@ -860,15 +893,16 @@ static pkv_status launch_prefill_tc_s(const PrefillParams& q, const CUtensorMap&
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tmK, tmV, q) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  return cudaLaunchKernelEx(&cfg, kern, tmQ, tmK, tmV, q) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 // One CTA per query tile when that fills at least half of the GPU (or other
 // work shares it); otherwise a cluster of two per tile, each taking half of
 // the key tiles. Beside a decode grid (may_split false), the 64-key tiles.
 template <int D, int KV, bool QBF16>
-static pkv_status launch_prefill_tc_t(const PrefillParams& p, const CUtensorMap& tmK,
-                                      const CUtensorMap& tmV, cudaStream_t stream,
+static pkv_status launch_prefill_tc_t(const PrefillParams& p, const CUtensorMap& tmQ,
+                                      const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                      cudaStream_t stream,
                                       bool may_split) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PKV_ERR_CUDA;
@@ -882,25 +916,26 @@ static pkv_status launch_prefill_tc_t(const PrefillParams& p, const CUtensorMap&
   PrefillParams q = p;
   q.q_tile = kTcRows / p.G;
   const int64_t ctas = (int64_t)((q.max_q_len + q.q_tile - 1) / q.q_tile) * q.Hkv * q.num_seqs;
-  if (!may_split) return launch_prefill_tc_s<D, KV, QBF16, 1, false>(q, tmK, tmV, stream, dev);
+  if (!may_split) return launch_prefill_tc_s<D, KV, QBF16, 1, false>(q, tmQ, tmK, tmV, stream, dev);
   if (2 * ctas <= n_sms)
-    return launch_prefill_tc_s<D, KV, QBF16, 2, true>(q, tmK, tmV, stream, dev);
-  return launch_prefill_tc_s<D, KV, QBF16, 1, true>(q, tmK, tmV, stream, dev);
+    return launch_prefill_tc_s<D, KV, QBF16, 2, true>(q, tmQ, tmK, tmV, stream, dev);
+  return launch_prefill_tc_s<D, KV, QBF16, 1, true>(q, tmQ, tmK, tmV, stream, dev);
 }
 
 template <int D>
 static pkv_status launch_prefill_tc_d(const PrefillParams& p, pkv_dtype q_dtype,
-                                      pkv_dtype kv_dtype, const CUtensorMap& tmK,
-                                      const CUtensorMap& tmV, cudaStream_t stream,
+                                      pkv_dtype kv_dtype, const CUtensorMap& tmQ,
+                                      const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                      cudaStream_t stream,
                                       bool may_split) {
   if (kv_dtype == PKV_BF16)
-    return launch_prefill_tc_t<D, KV_BF16, true>(p, tmK, tmV, stream, may_split);
+    return launch_prefill_tc_t<D, KV_BF16, true>(p, tmQ, tmK, tmV, stream, may_split);
   if (kv_dtype == PKV_F16)
-    return launch_prefill_tc_t<D, KV_F16, false>(p, tmK, tmV, stream, may_split);
+    return launch_prefill_tc_t<D, KV_F16, false>(p, tmQ, tmK, tmV, stream, may_split);
   if constexpr (D <= 128) {
     return q_dtype == PKV_BF16
-               ? launch_prefill_tc_t<D, KV_E4M3, true>(p, tmK, tmV, stream, may_split)
-               : launch_prefill_tc_t<D, KV_E4M3, false>(p, tmK, tmV, stream, may_split);
+               ? launch_prefill_tc_t<D, KV_E4M3, true>(p, tmQ, tmK, tmV, stream, may_split)
+               : launch_prefill_tc_t<D, KV_E4M3, false>(p, tmQ, tmK, tmV, stream, may_split);
   }
   return PKV_ERR_UNSUPPORTED;
 }
@@ -911,13 +946,13 @@ bool prefill_tc_supported(int head_dim, pkv_dtype kv_dtype) {
 }
 
 pkv_status launch_prefill_tc(const PrefillParams& p, int head_dim, pkv_dtype q_dtype,
-                             pkv_dtype kv_dtype, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                             cudaStream_t stream, bool may_split) {
+                             pkv_dtype kv_dtype, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                             const CUtensorMap& tmV, cudaStream_t stream, bool may_split) {
   if (head_dim == 256)
-    return launch_prefill_tc_d<256>(p, q_dtype, kv_dtype, tmK, tmV, stream, may_split);
+    return launch_prefill_tc_d<256>(p, q_dtype, kv_dtype, tmQ, tmK, tmV, stream, may_split);
   if (head_dim == 128)
-    return launch_prefill_tc_d<128>(p, q_dtype, kv_dtype, tmK, tmV, stream, may_split);
-  return launch_prefill_tc_d<64>(p, q_dtype, kv_dtype, tmK, tmV, stream, may_split);
+    return launch_prefill_tc_d<128>(p, q_dtype, kv_dtype, tmQ, tmK, tmV, stream, may_split);
+  return launch_prefill_tc_d<64>(p, q_dtype, kv_dtype, tmQ, tmK, tmV, stream, may_split);
 }
 
 }  // namespace pkv

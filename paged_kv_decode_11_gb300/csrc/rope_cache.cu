@@ -32,7 +32,7 @@
 #include <cuda_bf16.h>
 #include "common.cuh"
 #include "kv_store.cuh"
-#include "launch.h"
+#include "launch_cache.h"
 
 namespace pkv {
 
