@@ -340,9 +340,13 @@ def test_prefill_one_cta_and_cluster_key_split(L, P_, dtype, Hq, Hkv, D, split, 
     assert_close(lse, wlse, LSE_TOL, "prefill lse")
 
 
-def test_prefill_several_sequences_in_one_call():
-    # three sequences with different chunk lengths and histories
-    c = _prefill_case(10, 10, 10, "bf16", "same", 8, 2, 128)
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (28, 4)])
+def test_prefill_several_sequences_in_one_call(Hq, Hkv):
+    # three sequences with different chunk lengths and histories; a query
+    # tile of one sequence spans the next sequence's rows of q (G = 4: 32
+    # tokens a tile; G = 7: 18 tokens, 126 of 128 rows), which its output
+    # must leave alone
+    c = _prefill_case(10, 10, 10, "bf16", "same", Hq, Hkv, 128)
     kc, vc = product_cache(c)
     ko, vo = oracle_cache(c)
     # reuse the two decode sequences as extra prefill sequences: their chunk
