@@ -368,8 +368,9 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
     if (u + NSS < n_tiles) issue(u + NSS);
   };
   if (warp == Cfg::W_K) {
-    // the K producer sets up the barriers; the producers start the first tiles
-    // right away, while the other warps load the query tile and allocate tensor memory
+    // the first K producer sets up the barriers and starts the query tile's
+    // load; the K producers then start K tile 0 (below), while the other warps
+    // allocate tensor memory
     if (lane == 0) {
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
@@ -425,7 +426,7 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
 
   // ---- query tile into shared memory. 16-bit cache: by TMA (issued above), the
   // last softmax group zeroing the rows no pair uses; rows of tokens past the
-  // chunk hold the next tokens' queries, and their keys are all masked. E4M3
+  // chunk hold the next tokens' queries (their results are never stored). E4M3
   // cache: loaded (and scaled to f16) by the last softmax group, rows past the
   // chunk zero ----------------------------------------------------------------------
   const int grp = warp >> 2;                            // softmax group (warps 0 .. 4 NG - 1)
