@@ -98,7 +98,7 @@ typedef enum { PKV_F16 = 0, PKV_BF16 = 1, PKV_FP8_E4M3 = 2 } pkv_dtype;
 #define PKV_DEVERR_SLOT       0x2u  /* slot >= num_blocks * block_size */
 #define PKV_DEVERR_SEQ_LEN    0x4u  /* seq_len < 0 or above the stated maximum */
 #define PKV_DEVERR_TIMEOUT    0x8u  /* a bounded wait on an async copy gave up */
-#define PKV_DEVERR_QLEN       0x10u /* prefill: chunk longer than its context */
+#define PKV_DEVERR_QLEN       0x10u /* prefill: chunk longer than its context, or outside q's rows */
 #define PKV_DEVERR_POSITION   0x20u /* rotary: position outside [0, max_position) */
 #define PKV_DEVERR_COUNTER    0x40u /* decode: workspace counters were not zero */
 
@@ -255,7 +255,8 @@ pkv_status paged_attn_decode_noalloc_reset(void* stream);
  *   bottom right). Same scores, scales and output dtype as decode.
  *   max_q_len: upper bound on every L_n (sizes the grid).
  *   out_lse: optional fp32 [total_q_tokens, Hq].
- *   A chunk with L_n > seq_lens[n] sets PKV_DEVERR_QLEN and is skipped.
+ *   A chunk with L_n > seq_lens[n], or whose rows do not lie within the
+ *   total_q_tokens rows of q and out, sets PKV_DEVERR_QLEN and is skipped.
  *   Launch: one CTA per tile of query rows; when those would occupy at most
  *   half of the SMs, a cluster of two CTAs per tile, each over half of the
  *   tile's keys, merged by log-sum-exp on chip (tensor-core kernel: 16-bit

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(HERE, "libpkv.so")
 PKV_F16, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
           3: "workspace missing or too small", 4: "CUDA error", 5: "device-side check failed"}
-DEVERR_BITS = {0x1: "block id", 0x2: "slot", 0x4: "seq_len", 0x8: "timeout", 0x10: "chunk length",
+DEVERR_BITS = {0x1: "block id", 0x2: "slot", 0x4: "seq_len", 0x8: "timeout", 0x10: "chunk length or rows",
                0x20: "rotary position", 0x40: "workspace counters not zero"}
 
 # Every symbol include/pkv.h declares.

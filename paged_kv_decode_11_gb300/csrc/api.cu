@@ -375,6 +375,7 @@ pkv_status prefill_setup(void* out, const void* q, pkv_dtype q_dtype, const void
   p.num_blocks = num_blocks;
   p.max_q_len = max_q_len;
   p.q_tile = prefill_q_tile(G);
+  p.q_rows = q_rows;
   p.ppb_shift = shift;
   p.qk_scale_log2 = scale * 1.4426950408889634f;  // log2(e)
   return PKV_OK;

@@ -16,6 +16,7 @@ struct PrefillParams {
   float* out_lse;
   unsigned int* err;
   int num_seqs, Hq, Hkv, G, max_blocks, num_blocks, max_q_len, q_tile;
+  int q_rows;                 // rows of q and out; a chunk outside them is flagged
   int ppb_shift;              // log2(block_size / 16)
   float qk_scale_log2;
 };

@@ -223,7 +223,9 @@ __global__ void __launch_bounds__(PrefillTcCfg<D, NST, KV == KV_E4M3, ALONE>::TH
   const int q0 = p.cu_q_lens[n];
   const int L = p.cu_q_lens[n + 1] - q0;
   const int ctx = p.seq_lens[n];
-  if (L < 0 || L > ctx || ctx > ((p.max_blocks * kBS) << p.ppb_shift)) {
+  // a chunk longer than its context, or whose rows are not rows of q and out
+  if (L < 0 || L > ctx || q0 < 0 || q0 > p.q_rows - L ||
+      ctx > ((p.max_blocks * kBS) << p.ppb_shift)) {
     if (tid == 0 && qt == 0 && h == 0) atomicOr(p.err, PKV_DEVERR_QLEN);
     return;
   }

@@ -395,6 +395,31 @@ def test_prefill_flags_chunk_longer_than_context():
     assert P.pkv_get_device_error() & 0x10
 
 
+def test_prefill_flags_chunk_outside_q_rows():
+    # the second sequence's chunk claims rows 5 .. 44 of a 30-row q and out:
+    # flagged and skipped, nothing read or written past the rows; the first
+    # sequence's chunk (rows 0 .. 4) is computed as usual
+    c = _prefill_case(13, 40, 30, "bf16", "same", 8, 2, 128)
+    kc, vc = product_cache(c)
+    ko, vo = oracle_cache(c)
+    width = max(c.block_tables.shape[1], c.prefill.block_tables.shape[1])
+    tables = np.zeros((2, width), np.int32)
+    tables[0, :c.block_tables.shape[1]] = c.block_tables[0]
+    tables[1, :c.prefill.block_tables.shape[1]] = c.prefill.block_tables[0]
+    seq_lens = np.array([c.seq_lens[0], c.prefill.seq_lens[0]], np.int32)
+    assert seq_lens[1] >= 40                              # the chunk fits its context
+    cu = np.array([0, 5, 45], np.int32)
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn((30, c.Hq, c.D), generator=g).to(torch.bfloat16)
+    out = torch.zeros_like(q).cuda()
+    P.paged_attn_prefill_chunk(out, dev(q), kc, vc, dev(tables), dev(seq_lens), dev(cu),
+                               float(c.scale), 40)
+    assert P.pkv_get_device_error() & 0x10
+    want, _ = O.prefill_chunk(q[:5], ko, vo, tables[:1], seq_lens[:1], cu[:2], c.scale)
+    assert_close(out[:5], want, 1e-2, "the chunk inside q's rows")
+    assert not out[5:].any(), "rows of the flagged chunk were written"
+
+
 # ---- the mixed continuous-batching step ----------------------------------------------
 
 def test_mixed_step_vs_oracle():
